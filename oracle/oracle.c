@@ -1,0 +1,273 @@
+/*
+ * oracle.c -- plain fp64 CPU reference for multi-head scaled dot-product
+ * attention.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may call, link or
+ * load this file; only the test suite, the smoke check and the benchmark's
+ * CPU-baseline leg use it.  It shares no code, header, table or helper with
+ * the CUDA library.
+ *
+ * What it computes (the definition, written out, no blocking or fusion):
+ *
+ *   Attention(Q, K, V) = softmax(Q K^T / sqrt(d_k) + M) V
+ *     -- "How Transformers Work" (worksonmygpu.com), section "Scaled
+ *        dot-product attention", steps 1-4; "The Transformer"
+ *        (hoshank.vercel.app), section "The Mathematics", first equation.
+ *   M is an additive mask: 0 where key j is visible from query i, -inf where
+ *   it is blocked, so that a blocked key gets weight exactly 0
+ *     -- "The Transformer" (rayaq.ca), section "Masks: who may look at whom".
+ *   Causal: key j is blocked for query i when j > i (the strict upper
+ *   triangle, as in the printed 4x4 mask of that section).
+ *   Key padding: key j is blocked for every query of batch item b when
+ *   j >= key_lengths[b] (one row of the mask per batch item, same section).
+ *
+ *   MultiHead(x_q, x_kv) = Concat(head_1, ..., head_h) W^O,
+ *   head_i = Attention(x_q W^Q_i, x_kv W^K_i, x_kv W^V_i)
+ *     -- "The Transformer" (hoshank.vercel.app), "The Mathematics", the
+ *        multi-head equation; "32 Transformer" (ml-canon-en), section
+ *        "PyTorch Implementation": the projections are x @ W with W stored
+ *        [d_model, d_model], head i is column block [i*d_k, (i+1)*d_k) of the
+ *        projection, and the heads are concatenated in head order before
+ *        the product with W^O.
+ *
+ * Readings where the pages leave a step open:
+ *   - scale == 0 selects the default 1/sqrt(d_k); any other value is used
+ *     as given (the pages only ever use 1/sqrt(d_k)).
+ *   - the row maximum is subtracted before exp; softmax is invariant under
+ *     that shift, so the result is the definition's.
+ *   - a query row with no visible key has no defined softmax (0/0); the
+ *     oracle writes NaN there and returns a nonzero status.
+ *   - no bias terms (the pages' formula and snippet have none).
+ *
+ * All arithmetic is IEEE double.  Inputs are double arrays (the exact values
+ * the GPU reads, upcast from bf16 or fp32 by the caller).
+ */
+#include <math.h>
+#include <stddef.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORACLE_MASK_CAUSAL 1
+#define ORACLE_MASK_KEY_PADDING 2
+
+/* Additive mask entry M[i][j] for query i, key j (0 or -inf). */
+static double mask_entry(int i, int j, int mask_kind, int len_b)
+{
+    if ((mask_kind & ORACLE_MASK_CAUSAL) && j > i)
+        return -INFINITY;
+    if ((mask_kind & ORACLE_MASK_KEY_PADDING) && j >= len_b)
+        return -INFINITY;
+    return 0.0;
+}
+
+/*
+ * One query row of attention.
+ *   q      : d values
+ *   K, V   : Lk rows, row j at K + j*ldk / V + j*ldv, d values each
+ *   w      : out, Lk attention weights (softmax of the masked scores)
+ *   o      : out, d values, o[c] = sum_j w[j] * V[j][c]
+ * Returns 0, or 1 when the row has no visible key (w and o become NaN).
+ */
+static int attend_row(const double *q, const double *K, ptrdiff_t ldk,
+                      const double *V, ptrdiff_t ldv, int Lk, int d,
+                      double scale, int i, int mask_kind, int len_b,
+                      double *w, double *o)
+{
+    /* scores s_j = scale * <q, k_j> + M_ij */
+    for (int j = 0; j < Lk; ++j) {
+        double dot = 0.0;
+        for (int c = 0; c < d; ++c)
+            dot += q[c] * K[(ptrdiff_t)j * ldk + c];
+        w[j] = scale * dot + mask_entry(i, j, mask_kind, len_b);
+    }
+    /* row maximum */
+    double m = -INFINITY;
+    for (int j = 0; j < Lk; ++j)
+        if (w[j] > m)
+            m = w[j];
+    if (m == -INFINITY) {
+        for (int j = 0; j < Lk; ++j)
+            w[j] = NAN;
+        for (int c = 0; c < d; ++c)
+            o[c] = NAN;
+        return 1;
+    }
+    /* softmax: exp(s_j - m) / sum_k exp(s_k - m); exp(-inf) is exactly 0 */
+    double Z = 0.0;
+    for (int j = 0; j < Lk; ++j) {
+        w[j] = exp(w[j] - m);
+        Z += w[j];
+    }
+    for (int j = 0; j < Lk; ++j)
+        w[j] = w[j] / Z;
+    /* weighted sum of value rows */
+    for (int c = 0; c < d; ++c)
+        o[c] = 0.0;
+    for (int j = 0; j < Lk; ++j)
+        for (int c = 0; c < d; ++c)
+            o[c] += w[j] * V[(ptrdiff_t)j * ldv + c];
+    return 0;
+}
+
+static double resolve_scale(double scale, int d)
+{
+    return scale == 0.0 ? 1.0 / sqrt((double)d) : scale;
+}
+
+static int len_of(const int32_t *key_lengths, int mask_kind, int b, int Lk)
+{
+    return (mask_kind & ORACLE_MASK_KEY_PADDING) ? key_lengths[b] : Lk;
+}
+
+/*
+ * Scaled dot-product attention over [B, H, L, d] tensors.
+ *   Q [B,H,Lq,d], K [B,H,Lk,d], V [B,H,Lk,d]  ->  O [B,H,Lq,d]
+ *   W (optional, may be NULL) receives the weights [B,H,Lq,Lk].
+ * Returns the number of rows that had no visible key.
+ */
+int oracle_sdpa(const double *Q, const double *K, const double *V, double *O,
+                double *W, int B, int H, int Lq, int Lk, int d, double scale,
+                int mask_kind, const int32_t *key_lengths, int nthreads)
+{
+    const double sc = resolve_scale(scale, d);
+    int bad = 0;
+#ifdef _OPENMP
+    if (nthreads > 0)
+        omp_set_num_threads(nthreads);
+#endif
+    (void)nthreads;
+#pragma omp parallel for schedule(dynamic) reduction(+ : bad)
+    for (long bh = 0; bh < (long)B * H; ++bh) {
+        const int b = (int)(bh / H);
+        const int len_b = len_of(key_lengths, mask_kind, b, Lk);
+        const double *Qh = Q + (size_t)bh * Lq * d;
+        const double *Kh = K + (size_t)bh * Lk * d;
+        const double *Vh = V + (size_t)bh * Lk * d;
+        double *wrow = (double *)malloc(sizeof(double) * (size_t)(Lk > 0 ? Lk : 1));
+        for (int i = 0; i < Lq; ++i) {
+            bad += attend_row(Qh + (size_t)i * d, Kh, d, Vh, d, Lk, d, sc, i,
+                              mask_kind, len_b, wrow, O + ((size_t)bh * Lq + i) * d);
+            if (W)
+                memcpy(W + ((size_t)bh * Lq + i) * Lk, wrow, sizeof(double) * (size_t)Lk);
+        }
+        free(wrow);
+    }
+    return bad;
+}
+
+/*
+ * The same attention, for a list of query rows only (for workloads whose
+ * full output is too costly on the CPU).  rows[r] = (b*H + h)*Lq + i.
+ * O_rows receives nrows x d values, row r for rows[r].
+ */
+int oracle_sdpa_rows(const double *Q, const double *K, const double *V,
+                     double *O_rows, const int64_t *rows, int nrows, int B,
+                     int H, int Lq, int Lk, int d, double scale, int mask_kind,
+                     const int32_t *key_lengths, int nthreads)
+{
+    const double sc = resolve_scale(scale, d);
+    int bad = 0;
+#ifdef _OPENMP
+    if (nthreads > 0)
+        omp_set_num_threads(nthreads);
+#endif
+    (void)nthreads;
+    (void)B;
+#pragma omp parallel for schedule(dynamic) reduction(+ : bad)
+    for (int r = 0; r < nrows; ++r) {
+        const int64_t bh = rows[r] / Lq;
+        const int i = (int)(rows[r] % Lq);
+        const int b = (int)(bh / H);
+        const int len_b = len_of(key_lengths, mask_kind, b, Lk);
+        double *wrow = (double *)malloc(sizeof(double) * (size_t)(Lk > 0 ? Lk : 1));
+        bad += attend_row(Q + (size_t)rows[r] * d, K + (size_t)bh * Lk * d, d,
+                          V + (size_t)bh * Lk * d, d, Lk, d, sc, i, mask_kind,
+                          len_b, wrow, O_rows + (size_t)r * d);
+        free(wrow);
+    }
+    return bad;
+}
+
+/* Y[M, N] = X[M, Kd] @ W[Kd, N], all row-major, plain triple loop. */
+static void matmul(const double *X, const double *Wt, double *Y, long M, int Kd, int N)
+{
+#pragma omp parallel for schedule(static)
+    for (long m = 0; m < M; ++m) {
+        for (int n = 0; n < N; ++n) {
+            double acc = 0.0;
+            for (int k = 0; k < Kd; ++k)
+                acc += X[(size_t)m * Kd + k] * Wt[(size_t)k * N + n];
+            Y[(size_t)m * N + n] = acc;
+        }
+    }
+}
+
+/*
+ * Multi-head attention layer forward (no biases).
+ *   x_q [B,Lq,D], x_kv [B,Lk,D], Wq/Wk/Wv/Wo [D,D] (y = x @ W)
+ *   out [B,Lq,D]
+ * Head i uses columns [i*d, (i+1)*d) of the projections, d = D/h, and the
+ * default scale 1/sqrt(d).  Returns -1 when D % h != 0, else the number of
+ * query rows with no visible key.
+ */
+int oracle_mha(const double *x_q, const double *x_kv, const double *Wq,
+               const double *Wk, const double *Wv, const double *Wo,
+               double *out, int B, int Lq, int Lk, int D, int h,
+               int mask_kind, const int32_t *key_lengths, int nthreads)
+{
+    if (h <= 0 || D % h != 0)
+        return -1;
+    const int d = D / h;
+    const double sc = 1.0 / sqrt((double)d);
+#ifdef _OPENMP
+    if (nthreads > 0)
+        omp_set_num_threads(nthreads);
+#endif
+    (void)nthreads;
+    double *Qp = (double *)malloc(sizeof(double) * (size_t)B * Lq * D + 8);
+    double *Kp = (double *)malloc(sizeof(double) * (size_t)B * Lk * D + 8);
+    double *Vp = (double *)malloc(sizeof(double) * (size_t)B * Lk * D + 8);
+    double *ctx = (double *)malloc(sizeof(double) * (size_t)B * Lq * D + 8);
+    /* projections: Q = x_q Wq, K = x_kv Wk, V = x_kv Wv */
+    matmul(x_q, Wq, Qp, (long)B * Lq, D, D);
+    matmul(x_kv, Wk, Kp, (long)B * Lk, D, D);
+    matmul(x_kv, Wv, Vp, (long)B * Lk, D, D);
+    /* per head: attention on column block [hh*d, (hh+1)*d); the head's
+     * output lands in the same column block of ctx (the concatenation) */
+    int bad = 0;
+#pragma omp parallel for schedule(dynamic) reduction(+ : bad)
+    for (long bh = 0; bh < (long)B * h; ++bh) {
+        const int b = (int)(bh / h);
+        const int hh = (int)(bh % h);
+        const int len_b = len_of(key_lengths, mask_kind, b, Lk);
+        double *wrow = (double *)malloc(sizeof(double) * (size_t)(Lk > 0 ? Lk : 1));
+        for (int i = 0; i < Lq; ++i) {
+            const double *q = Qp + ((size_t)b * Lq + i) * D + (size_t)hh * d;
+            const double *Kh = Kp + (size_t)b * Lk * D + (size_t)hh * d;
+            const double *Vh = Vp + (size_t)b * Lk * D + (size_t)hh * d;
+            double *o = ctx + ((size_t)b * Lq + i) * D + (size_t)hh * d;
+            bad += attend_row(q, Kh, D, Vh, D, Lk, d, sc, i, mask_kind, len_b, wrow, o);
+        }
+        free(wrow);
+    }
+    /* out = Concat(heads) Wo */
+    matmul(ctx, Wo, out, (long)B * Lq, D, D);
+    free(Qp);
+    free(Kp);
+    free(Vp);
+    free(ctx);
+    return bad;
+}
+
+int oracle_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

@@ -1,0 +1,367 @@
+"""Pins for the fp64 oracle: facts fixed by the pages and by mathematics,
+none of which re-types the oracle's own formula.
+
+Each ``pin_*`` takes an ``oracle.Oracle`` and raises AssertionError when the
+oracle disagrees.  ``tests/test_oracle_pins.py`` runs them on the oracle;
+``tests/test_oracle_mutants.py`` runs them on deliberately broken copies of
+the oracle and requires every copy to fail at least one pin.
+
+Sources of the pinned facts:
+  - rows of weights sum to 1, weights >= 0: "32 Transformer" (ml-canon-en),
+    PyTorch snippet comment; "The Transformer" (hoshank.vercel.app), symbol
+    table of the attention equation.
+  - the printed 4x4 causal mask and "-inf gives weight exactly 0":
+    "The Transformer" (rayaq.ca), "Masks: who may look at whom".
+  - key padding masks keys per batch item: same section.
+  - permutation: swapping two words swaps their outputs and nothing else:
+    "The Transformer" (rayaq.ca), "Embeddings and positions".
+  - score variance d_k before scaling and 1 after: "32 Transformer",
+    "Why we divide by sqrt(dk)"; hoshank, "The Mathematics".
+  - one-hot collapse of sharply peaked rows: rayaq.ca, "Worked example".
+  - the multi-head assembly (projection x @ W, head i = column block i,
+    concat, @ Wo): "32 Transformer", "PyTorch Implementation"; hoshank,
+    multi-head equation.
+  - library routines: torch's CPU float64 ``scaled_dot_product_attention``
+    and ``multi_head_attention_forward`` (an independent implementation).
+"""
+from __future__ import annotations
+
+import math
+import os
+
+import numpy as np
+
+from oracle import MASK_CAUSAL, MASK_KEY_PADDING, MASK_NONE
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+def _qkv(rng, B, H, Lq, Lk, d):
+    return (rng.standard_normal((B, H, Lq, d)), rng.standard_normal((B, H, Lk, d)),
+            rng.standard_normal((B, H, Lk, d)))
+
+
+def _allclose(a, b, tol, what):
+    a, b = np.asarray(a), np.asarray(b)
+    assert a.shape == b.shape, f"{what}: shape {a.shape} vs {b.shape}"
+    assert np.all(np.isfinite(a)), f"{what}: non-finite values"
+    err = float(np.max(np.abs(a - b))) if a.size else 0.0
+    assert err <= tol, f"{what}: max|err| {err:.3e} > {tol:.1e}"
+
+
+def read_mask_fixture():
+    rows = []
+    with open(os.path.join(GOLDEN, "causal_mask_4x4.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            rows.append([float(t) for t in line.split()])
+    return np.array(rows)
+
+
+# ---------------------------------------------------------------- SDPA pins
+
+def pin_rows_sum_to_one(orc):
+    rng = _rng(1)
+    B, H, Lq, Lk, d = 2, 3, 5, 7, 8
+    Q, K, V = _qkv(rng, B, H, Lq, Lk, d)
+    lens = np.array([3, 7], dtype=np.int32)
+    for mk in (MASK_NONE, MASK_KEY_PADDING):
+        _, W = orc.sdpa(Q, K, V, mask_kind=mk, key_lengths=lens, return_weights=True)
+        assert np.all(W >= 0.0), "negative weight"
+        _allclose(W.sum(-1), np.ones((B, H, Lq)), 1e-12, "row sums")
+    Q, K, V = _qkv(rng, B, H, 6, 6, d)
+    _, W = orc.sdpa(Q, K, V, mask_kind=MASK_CAUSAL, return_weights=True)
+    assert np.all(W >= 0.0)
+    _allclose(W.sum(-1), np.ones((B, H, 6)), 1e-12, "causal row sums")
+
+
+def pin_printed_causal_mask(orc):
+    mask = read_mask_fixture()
+    assert mask.shape == (4, 4)
+    rng = _rng(2)
+    for trial in range(5):
+        Q, K, V = _qkv(rng, 1, 2, 4, 4, 16)
+        _, W = orc.sdpa(Q * (1 + 3 * trial), K, V, mask_kind=MASK_CAUSAL,
+                        return_weights=True)
+        blocked = np.isneginf(mask)
+        for h in range(2):
+            assert np.all(W[0, h][blocked] == 0.0), "blocked key has nonzero weight"
+            assert np.all(W[0, h][~blocked] > 0.0), "visible key has zero weight"
+
+
+def pin_causal_future_independence(orc):
+    rng = _rng(3)
+    B, H, L, d = 2, 2, 9, 8
+    Q, K, V = _qkv(rng, B, H, L, L, d)
+    O = orc.sdpa(Q, K, V, mask_kind=MASK_CAUSAL)
+    for i in (0, 3, 7):
+        K2, V2 = K.copy(), V.copy()
+        K2[:, :, i + 1:] = rng.standard_normal(K2[:, :, i + 1:].shape) * 5
+        V2[:, :, i + 1:] = rng.standard_normal(V2[:, :, i + 1:].shape) * 5
+        O2 = orc.sdpa(Q, K2, V2, mask_kind=MASK_CAUSAL)
+        assert np.array_equal(O[:, :, : i + 1], O2[:, :, : i + 1]), \
+            f"row <= {i} depends on a future key"
+        if i + 1 < L:
+            assert not np.array_equal(O[:, :, i + 1:], O2[:, :, i + 1:])
+
+
+def pin_key_padding(orc):
+    rng = _rng(4)
+    B, H, Lq, Lk, d = 3, 2, 5, 8, 8
+    Q, K, V = _qkv(rng, B, H, Lq, Lk, d)
+    full = np.full(B, Lk, dtype=np.int32)
+    assert np.array_equal(orc.sdpa(Q, K, V, mask_kind=MASK_KEY_PADDING, key_lengths=full),
+                          orc.sdpa(Q, K, V)), "len = Lk differs from no mask"
+    lens = np.array([2, 5, 8], dtype=np.int32)
+    O = orc.sdpa(Q, K, V, mask_kind=MASK_KEY_PADDING, key_lengths=lens)
+    K2, V2 = K.copy(), V.copy()
+    for b, n in enumerate(lens):
+        K2[b, :, n:] = 7.0
+        V2[b, :, n:] = -9.0
+    O2 = orc.sdpa(Q, K2, V2, mask_kind=MASK_KEY_PADDING, key_lengths=lens)
+    assert np.array_equal(O, O2), "padded keys changed the output"
+    # and a padded key does matter once it is inside the length
+    O3 = orc.sdpa(Q, K2, V2, mask_kind=MASK_KEY_PADDING, key_lengths=lens + np.array([1, 1, 0], np.int32))
+    assert not np.array_equal(O[:2], O3[:2])
+
+
+def pin_single_visible_key(orc):
+    """One visible key: the output is that key's value row, exactly."""
+    rng = _rng(5)
+    B, H, Lq, Lk, d = 2, 3, 4, 6, 8
+    Q, K, V = _qkv(rng, B, H, Lq, Lk, d)
+    O = orc.sdpa(Q, K, V, mask_kind=MASK_KEY_PADDING, key_lengths=np.array([1, 1], np.int32))
+    for i in range(Lq):
+        assert np.array_equal(O[:, :, i], V[:, :, 0]), "len 1 is not V row 0"
+    Q, K, V = _qkv(rng, B, H, 5, 5, d)
+    O = orc.sdpa(Q, K, V, mask_kind=MASK_CAUSAL)
+    assert np.array_equal(O[:, :, 0], V[:, :, 0]), "causal row 0 is not V row 0"
+
+
+def pin_zero_query_is_mean(orc):
+    """q = 0: all scores equal, so the output is the mean of the visible values."""
+    rng = _rng(6)
+    B, H, L, d = 2, 2, 7, 8
+    _, K, V = _qkv(rng, B, H, L, L, d)
+    Q = np.zeros((B, H, L, d))
+    O = orc.sdpa(Q, K, V)
+    _allclose(O, np.broadcast_to(V.mean(axis=2, keepdims=True), O.shape), 1e-13, "uniform")
+    O = orc.sdpa(Q, K, V, mask_kind=MASK_CAUSAL)
+    prefix = np.cumsum(V, axis=2) / np.arange(1, L + 1)[None, None, :, None]
+    _allclose(O, prefix, 1e-13, "causal uniform")
+    lens = np.array([3, 6], np.int32)
+    O = orc.sdpa(Q, K, V, mask_kind=MASK_KEY_PADDING, key_lengths=lens)
+    for b, n in enumerate(lens):
+        _allclose(O[b], np.broadcast_to(V[b, :, :n].mean(axis=1, keepdims=True), O[b].shape),
+                  1e-13, "padding uniform")
+
+
+def pin_two_keys_logistic(orc):
+    """Two keys: the weights are (sigma(s0 - s1), sigma(s1 - s0)), sigma the
+    logistic function, with s_j = <q, k_j> / sqrt(d)."""
+    rng = _rng(7)
+    d = 16
+    Q, K, V = _qkv(rng, 1, 6, 3, 2, d)
+    O, W = orc.sdpa(Q, K, V, return_weights=True)
+    for h in range(6):
+        for i in range(3):
+            s0 = math.fsum(Q[0, h, i] * K[0, h, 0]) / math.sqrt(d)
+            s1 = math.fsum(Q[0, h, i] * K[0, h, 1]) / math.sqrt(d)
+            w0 = 1.0 / (1.0 + math.exp(s1 - s0))
+            assert abs(W[0, h, i, 0] - w0) <= 1e-14, "two-key weight"
+            assert abs(W[0, h, i, 1] - (1.0 - w0)) <= 1e-14
+            exp_o = w0 * V[0, h, 0] + (1.0 - w0) * V[0, h, 1]
+            _allclose(O[0, h, i], exp_o, 1e-14, "two-key output")
+
+
+def pin_one_hot_margin(orc):
+    """A key whose score beats every other by a margin g gets all but
+    (n-1)e^-g of the weight, so the output is that key's value row."""
+    rng = _rng(8)
+    d, Lk = 32, 10
+    for target in (0, 4, 9):
+        q = rng.standard_normal(d)
+        q /= np.linalg.norm(q)
+        K = rng.standard_normal((Lk, d)) * 0.01
+        gap = 30.0
+        K[target] = q * gap * math.sqrt(d)          # scaled score ~= gap
+        V = rng.standard_normal((Lk, d))
+        O = orc.sdpa(q[None, None, None], K[None, None], V[None, None])
+        bound = (Lk - 1) * math.exp(-gap + 2.0) * np.max(np.abs(V)) * 2
+        _allclose(O[0, 0, 0], V[target], bound, "one-hot")
+
+
+def pin_score_variance(orc):
+    """For i.i.d. N(0,1) q, k the raw score has variance d_k and the scaled
+    one variance 1.  With two keys the weight w0 = sigma(s0 - s1) exposes the
+    score difference, whose variance is 2 (scaled) or 2 d_k (unscaled)."""
+    rng = _rng(9)
+    N = 20000
+    for d in (64, 128):
+        Q, K, V = _qkv(rng, 1, N, 1, 2, d)
+        for scale, target in ((0.0, 2.0), (1.0, 2.0 * d)):
+            _, W = orc.sdpa(Q, K, V, scale=scale, return_weights=True)
+            diff = np.log(W[0, :, 0, 0]) - np.log(W[0, :, 0, 1])
+            var = float(np.var(diff))
+            rel_sd = math.sqrt((2.0 + 6.0 / d) / N)
+            assert abs(var / target - 1.0) <= 5 * rel_sd, \
+                f"d={d} scale={scale}: var {var:.4f} vs {target}"
+
+
+def pin_kv_permutation_and_shift(orc):
+    rng = _rng(10)
+    B, H, Lq, Lk, d = 2, 2, 5, 9, 8
+    Q, K, V = _qkv(rng, B, H, Lq, Lk, d)
+    O = orc.sdpa(Q, K, V)
+    perm = rng.permutation(Lk)
+    _allclose(orc.sdpa(Q, K[:, :, perm], V[:, :, perm]), O, 1e-13, "kv permutation")
+    w = rng.standard_normal(d) * 3
+    _allclose(orc.sdpa(Q, K + w, V), O, 1e-12, "key shift")
+
+
+def pin_torch_sdpa(orc):
+    """Library cross-check: torch's CPU float64 scaled_dot_product_attention."""
+    import torch
+    import torch.nn.functional as F
+    rng = _rng(11)
+    cases = [(2, 3, 17, 17, 16, MASK_NONE), (2, 2, 13, 13, 32, MASK_CAUSAL),
+             (3, 2, 11, 20, 8, MASK_KEY_PADDING), (1, 2, 19, 19, 64, MASK_CAUSAL | MASK_KEY_PADDING),
+             (2, 1, 5, 33, 128, MASK_NONE)]
+    for B, H, Lq, Lk, d, mk in cases:
+        Q, K, V = _qkv(rng, B, H, Lq, Lk, d)
+        lens = rng.integers(1, Lk + 1, size=B).astype(np.int32) if mk & MASK_KEY_PADDING else None
+        if mk & MASK_KEY_PADDING and mk & MASK_CAUSAL:
+            lens = np.maximum(lens, 1)
+        add = np.zeros((B, 1, Lq, Lk))
+        if mk & MASK_CAUSAL:
+            add += np.triu(np.full((Lq, Lk), -np.inf), 1)[None, None]
+        if mk & MASK_KEY_PADDING:
+            for b in range(B):
+                add[b, :, :, lens[b]:] = -np.inf
+        ref = F.scaled_dot_product_attention(torch.from_numpy(Q), torch.from_numpy(K),
+                                             torch.from_numpy(V),
+                                             attn_mask=torch.from_numpy(add)).numpy()
+        got = orc.sdpa(Q, K, V, mask_kind=mk, key_lengths=lens)
+        _allclose(got, ref, 1e-12, f"torch sdpa {B,H,Lq,Lk,d,mk}")
+    # explicit scale
+    Q, K, V = _qkv(rng, 1, 2, 6, 6, 16)
+    ref = F.scaled_dot_product_attention(torch.from_numpy(Q), torch.from_numpy(K),
+                                         torch.from_numpy(V), scale=0.3).numpy()
+    _allclose(orc.sdpa(Q, K, V, scale=0.3), ref, 1e-12, "explicit scale")
+
+
+def pin_sdpa_rows_match_full(orc):
+    rng = _rng(12)
+    B, H, L, d = 2, 3, 21, 16
+    Q, K, V = _qkv(rng, B, H, L, L, d)
+    for mk, lens in ((MASK_CAUSAL, None), (MASK_KEY_PADDING, np.array([4, 21], np.int32))):
+        full = orc.sdpa(Q, K, V, mask_kind=mk, key_lengths=lens)
+        rows = np.array([0, 5, 20, 21, 40, 62, 125], dtype=np.int64)
+        got = orc.sdpa_rows(Q, K, V, rows, mask_kind=mk, key_lengths=lens)
+        assert np.array_equal(got, full.reshape(-1, d)[rows]), "row sample differs"
+
+
+# ----------------------------------------------------------------- MHA pins
+
+def _mha_inputs(rng, B, Lq, Lk, D, cross=True):
+    xq = rng.standard_normal((B, Lq, D))
+    xkv = rng.standard_normal((B, Lk, D)) if cross else xq
+    Ws = [rng.standard_normal((D, D)) / math.sqrt(D) for _ in range(4)]
+    return xq, xkv, Ws
+
+
+def _torch_mha(xq, xkv, Ws, h, causal=False, lens=None):
+    import torch
+    import torch.nn.functional as F
+    Wq, Wk, Wv, Wo = (torch.from_numpy(np.ascontiguousarray(w.T)) for w in Ws)
+    D = xq.shape[-1]
+    q = torch.from_numpy(xq).transpose(0, 1)
+    kv = torch.from_numpy(xkv).transpose(0, 1)
+    Lq, Lk = xq.shape[1], xkv.shape[1]
+    attn_mask = None
+    if causal:
+        attn_mask = torch.triu(torch.full((Lq, Lk), float("-inf"), dtype=torch.float64), 1)
+    kpm = None
+    if lens is not None:
+        kpm = torch.arange(Lk)[None, :] >= torch.from_numpy(np.asarray(lens))[:, None]
+    out, _ = F.multi_head_attention_forward(
+        q, kv, kv, D, h, None, None, None, None, False, 0.0, Wo, None,
+        training=False, key_padding_mask=kpm, need_weights=False, attn_mask=attn_mask,
+        use_separate_proj_weight=True, q_proj_weight=Wq, k_proj_weight=Wk,
+        v_proj_weight=Wv)
+    return out.transpose(0, 1).numpy()
+
+
+def pin_mha_torch(orc):
+    """Library cross-check: torch.nn.functional.multi_head_attention_forward,
+    float64, separate projection weights (transposed: torch computes x W^T),
+    no biases."""
+    rng = _rng(20)
+    cases = [(2, 9, 9, 32, 4, MASK_NONE, False), (1, 12, 12, 48, 3, MASK_CAUSAL, False),
+             (2, 7, 13, 32, 2, MASK_KEY_PADDING, True), (3, 5, 11, 64, 8, MASK_NONE, True)]
+    for B, Lq, Lk, D, h, mk, cross in cases:
+        xq, xkv, Ws = _mha_inputs(rng, B, Lq, Lk, D, cross)
+        lens = rng.integers(1, Lk + 1, size=B).astype(np.int32) if mk & MASK_KEY_PADDING else None
+        ref = _torch_mha(xq, xkv, Ws, h, causal=bool(mk & MASK_CAUSAL), lens=lens)
+        got = orc.mha(xq, xkv, *Ws, h=h, mask_kind=mk, key_lengths=lens)
+        _allclose(got, ref, 1e-11, f"torch mha {B,Lq,Lk,D,h,mk}")
+
+
+def pin_mha_single_head_identity(orc):
+    """h = 1 and every W = I: the layer is SDPA(x, x, x) with scale 1/sqrt(D)."""
+    rng = _rng(21)
+    B, L, D = 2, 6, 16
+    x = rng.standard_normal((B, L, D))
+    I = np.eye(D)
+    got = orc.mha(x, x, I, I, I, I, h=1)
+    ref = orc.sdpa(x[:, None], x[:, None], x[:, None], scale=1.0 / math.sqrt(D))[:, 0]
+    _allclose(got, ref, 1e-13, "single head identity")
+
+
+def pin_mha_head_blocks(orc):
+    """out = sum_i head_i @ Wo[rows of block i], head_i = SDPA on column block i."""
+    rng = _rng(22)
+    B, Lq, Lk, D, h = 2, 5, 7, 24, 3
+    d = D // h
+    xq, xkv, (Wq, Wk, Wv, Wo) = _mha_inputs(rng, B, Lq, Lk, D)
+    got = orc.mha(xq, xkv, Wq, Wk, Wv, Wo, h=h)
+    acc = np.zeros((B, Lq, D))
+    for i in range(h):
+        blk = slice(i * d, (i + 1) * d)
+        head = orc.sdpa((xq @ Wq[:, blk])[:, None], (xkv @ Wk[:, blk])[:, None],
+                        (xkv @ Wv[:, blk])[:, None])[:, 0]
+        acc += head @ Wo[blk, :]
+    _allclose(got, acc, 1e-12, "head block decomposition")
+
+
+def pin_mha_permutation_equivariance(orc):
+    rng = _rng(23)
+    B, L, D, h = 2, 8, 32, 4
+    x, _, Ws = _mha_inputs(rng, B, L, L, D, cross=False)
+    out = orc.mha(x, x, *Ws, h=h)
+    perm = rng.permutation(L)
+    xp = x[:, perm]
+    _allclose(orc.mha(xp, xp, *Ws, h=h), out[:, perm], 1e-12, "permutation equivariance")
+
+
+def pin_mha_linearity(orc):
+    rng = _rng(24)
+    B, Lq, Lk, D, h = 1, 4, 6, 16, 2
+    xq, xkv, (Wq, Wk, Wv, Wo) = _mha_inputs(rng, B, Lq, Lk, D)
+    Wo2 = rng.standard_normal((D, D))
+    Wv2 = rng.standard_normal((D, D))
+    a = orc.mha(xq, xkv, Wq, Wk, Wv, Wo + Wo2, h=h)
+    b = orc.mha(xq, xkv, Wq, Wk, Wv, Wo, h=h) + orc.mha(xq, xkv, Wq, Wk, Wv, Wo2, h=h)
+    _allclose(a, b, 1e-12, "linear in Wo")
+    a = orc.mha(xq, xkv, Wq, Wk, Wv + Wv2, Wo, h=h)
+    b = orc.mha(xq, xkv, Wq, Wk, Wv, Wo, h=h) + orc.mha(xq, xkv, Wq, Wk, Wv2, Wo, h=h)
+    _allclose(a, b, 1e-12, "linear in Wv")
+
+
+ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -1,0 +1,51 @@
+"""Plant plausible mistakes in copies of the oracle (on the CPU) and require
+the pins to catch every one: a pin set that a dropped scale, an off-by-one
+mask, a transposed value index or a mis-ordered concat slips through is not
+pinning the oracle."""
+import os
+import re
+
+import pytest
+
+import oracle
+from tests.oracle_pins import ALL_PINS
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
+
+# (name, exact text in oracle.c, replacement).  Each text must occur once.
+MUTANTS = [
+    ("scale_dropped", "w[j] = scale * dot +", "w[j] = dot +"),
+    ("default_scale_1_over_d", "1.0 / sqrt((double)d) : scale", "1.0 / (double)d : scale"),
+    ("causal_off_by_one", "(mask_kind & ORACLE_MASK_CAUSAL) && j > i",
+     "(mask_kind & ORACLE_MASK_CAUSAL) && j >= i"),
+    ("padding_off_by_one", "(mask_kind & ORACLE_MASK_KEY_PADDING) && j >= len_b",
+     "(mask_kind & ORACLE_MASK_KEY_PADDING) && j > len_b"),
+    ("no_normalisation", "w[j] = w[j] / Z;", "w[j] = w[j];"),
+    ("value_dims_reversed", "o[c] += w[j] * V[(ptrdiff_t)j * ldv + c];",
+     "o[c] += w[j] * V[(ptrdiff_t)j * ldv + (d - 1 - c)];"),
+    ("max_not_subtracted_sign", "w[j] = exp(w[j] - m);", "w[j] = exp(m - w[j]);"),
+    ("heads_concat_reversed", "double *o = ctx + ((size_t)b * Lq + i) * D + (size_t)hh * d;",
+     "double *o = ctx + ((size_t)b * Lq + i) * D + (size_t)(h - 1 - hh) * d;"),
+    ("mha_scale_uses_dmodel", "const double sc = 1.0 / sqrt((double)d);\n#ifdef",
+     "const double sc = 1.0 / sqrt((double)D);\n#ifdef"),
+    ("key_proj_uses_wq", "matmul(x_kv, Wk, Kp,", "matmul(x_kv, Wq, Kp,"),
+    ("query_row_stride_wrong", "bad += attend_row(Qh + (size_t)i * d,",
+     "bad += attend_row(Qh + (size_t)(Lq - 1 - i) * d,"),
+]
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutant_is_caught(tmp_path, name, old, new):
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation site for {name} not unique"
+    mut_src = tmp_path / f"oracle_{name}.c"
+    mut_src.write_text(src.replace(old, new))
+    lib_path = oracle.build(str(mut_src), str(tmp_path / f"lib_{name}.so"))
+    orc = oracle.Oracle(oracle.load_library(lib_path))
+    caught = []
+    for pin in ALL_PINS:
+        try:
+            pin(orc)
+        except AssertionError:
+            caught.append(pin.__name__)
+    assert caught, f"mutant {name} passed every pin"
