@@ -1,0 +1,424 @@
+"""Benchmark of the attention hot path on GB300.
+
+Default step: one sdpa_forward over the long-context causal workload
+(B1, L32768, H32, d128, bf16, causal, 4 outlier dims per head scaled x8 in
+Q and K): rows a3-a7 of the path (QK^T, scale + mask, online softmax, P V,
+epilogue) in one fused kernel launch.  `value` is that workload's SDPA
+forward throughput in TFLOP/s (algorithmic flops: 4*d per unmasked
+query/key pair, 2*B*H*d*L*(L+1) for causal), summed over all ranks.
+
+Extra legs in the same JSON line:
+  e2e          the same metric through the public call with host (pinned)
+               buffers: H2D of Q/K/V and D2H of O inside the timed region
+  roofline     the fused kernel against the measured bf16 tensor peak
+  mha_layer    the whole layer (rows a1-a8: projections with head-split
+               stores, attention with the concat store, output projection)
+               in tokens/s, on the same shape (D = 4096, h = 32) and on the
+               base fp32 shape (B1 L128 D512 h8)
+  cpu_baseline the fp64 oracle on this host's cores on a bounded row sample
+
+Multi-GPU: the path has no exchange step, so N ranks run N replicas (one per
+GPU, weak scaling); the time is the max over ranks after a barrier.
+
+`--impl reference` times the CPU oracle (the reference arm of this build) on
+the same workload, metric and unit.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "SDPA fwd TFLOP/s and % of GB300 BF16 tensor peak; MHA layer tokens/s"
+NOMINAL_BF16_TFLOPS = 2250.0
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_BYTES = 129 * 1024 * 1024
+
+
+# ------------------------------------------------------------ host helpers
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK}, "measured"
+    except Exception:
+        return dict(FALLBACK), "fallback"
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def whole_job_value(units_per_rank: float, world: int, max_seconds: float) -> float:
+    """Throughput of the whole job: the units all ranks processed over the
+    slowest rank's time."""
+    return units_per_rank * world / max_seconds
+
+
+def max_over_ranks(x: float, device=None) -> float:
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples every 200 ms while active."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self._t = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            if self._t is not None:
+                self._t.join(timeout=2)
+
+    def summary(self):
+        sms, maxes, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sms.append(float(parts[0]))
+                maxes.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sms:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": max(maxes),
+                "reasons": sorted(reasons), "samples": len(sms)}
+
+
+def oracle_cpu_baseline(w, Q, K, V, lens, rows):
+    """Time the fp64 oracle (as it stands) on a row sample; TFLOP/s."""
+    import oracle
+    orc = oracle.default()
+    t0 = time.perf_counter()
+    orc.sdpa_rows(Q, K, V, rows, mask_kind=w.mask, key_lengths=lens)
+    dt = time.perf_counter() - t0
+    i = rows % w.Lq
+    if w.mask & 1:
+        pairs = float(np.sum(i + 1))
+    elif w.mask & 2:
+        pairs = float(np.sum(lens[(rows // w.Lq) // w.H]))
+    else:
+        pairs = float(rows.size) * w.Lk
+    flops = 4.0 * w.d * pairs
+    return flops / dt / 1e12, dt, orc.num_threads()
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def bench_sdpa(args, w, rank, world, local_rank):
+    import torch
+    import transformer_head_scaled_03_gb300 as mha
+    from transformer_head_scaled_03_gb300.inputs import sample_rows, sdpa_inputs
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    Q, K, V, lens, dims = sdpa_inputs(w)
+    to_bf16 = lambda a: torch.from_numpy(a).to(torch.bfloat16)
+    Qh, Kh, Vh = (to_bf16(a).pin_memory() for a in (Q, K, V))
+    lens_h = torch.from_numpy(lens).pin_memory() if lens is not None else None
+    Qd, Kd, Vd = (t.to(dev) for t in (Qh, Kh, Vh))
+    kl = lens_h.to(dev) if lens_h is not None else None
+    Od = torch.empty_like(Qd)
+    flops = w.flops(lens)
+    in_bytes = sum(t.numel() * t.element_size() for t in (Qd, Kd, Vd))
+    out_bytes = Od.numel() * Od.element_size()
+    flush = None
+    if in_bytes + out_bytes < 2 * L2_BYTES:
+        flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+
+    def step():
+        mha.sdpa_forward(Qd, Kd, Vd, mask_kind=w.mask, key_lengths=kl, out=Od)
+
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert mha.mha_check() == mha.MHA_OK
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clocks:
+        if flush is None:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(args.steps):
+                step()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            total_ms = e0.elapsed_time(e1)
+        else:
+            total_ms = 0.0
+            for _ in range(args.steps):
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                step()
+                e1.record(stream)
+                torch.cuda.synchronize()
+                total_ms += e0.elapsed_time(e1)
+    barrier()
+    torch.cuda.synchronize()
+    st = mha.mha_check()
+    if st != mha.MHA_OK:
+        raise RuntimeError(f"device error during timing: {mha.status_string(st)}")
+    max_s = max_over_ranks(total_ms / 1e3, dev)
+    per_step = max_s / args.steps
+    value = whole_job_value(flops * args.steps, world, max_s) / 1e12
+    kernel_tflops = flops / (total_ms / 1e3 / args.steps) / 1e12  # this rank's kernel
+
+    # end to end through the public call from pinned host buffers
+    bufs = {}
+    for _ in range(2):
+        mha.sdpa_forward_host(Qh, Kh, Vh, mask_kind=w.mask, lengths_h=lens_h, bufs=bufs)
+    torch.cuda.synchronize()
+    barrier()
+    e2e_steps = max(2, min(args.steps, 5))
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        Oh = mha.sdpa_forward_host(Qh, Kh, Vh, mask_kind=w.mask, lengths_h=lens_h, bufs=bufs)
+        torch.cuda.current_stream().synchronize()
+        float(Oh[0, 0, 0, 0])  # read the result on the host
+    e2e_s = max_over_ranks(time.perf_counter() - t0, dev)
+    h2d = in_bytes + (lens_h.numel() * 4 if lens_h is not None else 0)
+    e2e = {"value": round(whole_job_value(flops * e2e_steps, world, e2e_s) / 1e12, 2),
+           "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": out_bytes,
+           "ms_per_step": round(e2e_s / e2e_steps * 1e3, 3)}
+    del bufs
+    return dict(value=value, per_step=per_step, kernel_tflops=kernel_tflops, flops=flops,
+                clocks=clocks.summary(), e2e=e2e, Q=Q, K=K, V=V, lens=lens, dims=dims,
+                l2="inputs larger than L2" if flush is None else "L2 flushed between steps")
+
+
+def bench_mha_layer(w_shape, dtype_name, steps, warmup, local_rank, seed_w=None):
+    """Tokens/s of one mha_forward (all rows a1-a8) on the given shape."""
+    import torch
+    import transformer_head_scaled_03_gb300 as mha
+    from transformer_head_scaled_03_gb300.inputs import Draws
+
+    B, L, D, h = w_shape
+    dev = torch.device("cuda", local_rank)
+    dtype = torch.bfloat16 if dtype_name == "bf16" else torch.float32
+    g = Draws(seed_w if seed_w is not None else 0x5EED0100 + D)
+    mk = lambda a: torch.from_numpy(a).to(dtype).to(dev)
+    x = mk(g.normal((B, L, D), dtype=dtype_name))
+    Ws = [mk(g.normal((D, D), std=1.0 / math.sqrt(D), dtype=dtype_name)) for _ in range(4)]
+    out = torch.empty_like(x)
+    handle = mha.mha_create(D, dtype, B, L, L)
+    try:
+        def step():
+            mha.mha_forward(handle, x, x, *Ws, h=h, out=out)
+        for _ in range(warmup):
+            step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            step()
+        e1.record()
+        torch.cuda.synchronize()
+        st = mha.mha_check(handle)
+        if st != mha.MHA_OK:
+            raise RuntimeError(mha.status_string(st))
+        ms = e0.elapsed_time(e1) / steps
+    finally:
+        handle.close()
+    d = D // h
+    proj_flops = 4 * 2.0 * B * L * D * D
+    attn_flops = 4.0 * B * h * L * L * d
+    return {"shape": {"B": B, "L": L, "D": D, "h": h, "dtype": dtype_name, "mask": "none"},
+            "tokens_per_s": round(B * L / (ms / 1e3), 1), "ms_per_layer": round(ms, 4),
+            "tflops": round((proj_flops + attn_flops) / (ms / 1e3) / 1e12, 2),
+            "gpu_launches_per_layer": 3}
+
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+    from transformer_head_scaled_03_gb300.inputs import WORKLOADS, sample_rows
+    import __graft_entry__
+
+    rank, world, local_rank = dist_env()
+    if world > 1:
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group(backend="nccl")
+    __graft_entry__.build()
+    w = WORKLOADS[args.workload]
+    r = bench_sdpa(args, w, rank, world, local_rank)
+    peaks, peak_src = measured_peaks()
+
+    mha_layer = None
+    if not args.skip_mha:
+        mha_layer = [bench_mha_layer((w.B, w.Lq, w.H * w.d, w.H), "bf16", 3, 2, local_rank),
+                     bench_mha_layer((1, 128, 512, 8), "f32", 50, 5, local_rank,
+                                     seed_w=WORKLOADS[1].seed)]
+
+    cpu = None
+    if rank == 0 and not args.skip_cpu:
+        rows = sample_rows(w.B, w.H, w.Lq, args.cpu_rows_per_head, seed=w.seed + 3000,
+                           must=())
+        tf, dt, cores = oracle_cpu_baseline(w, r["Q"], r["K"], r["V"], r["lens"], rows)
+        cpu = {"value": round(tf, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+               "seconds": round(dt, 2),
+               "sample": f"{rows.size} query rows ({args.cpu_rows_per_head} per head, all "
+                         f"{w.B * w.H} heads, seeded) of the same workload, fp64"}
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+    ach = r["kernel_tflops"]
+    peak = peaks["bf16_tflops"]
+    line = {
+        "metric": METRIC,
+        "value": round(r["value"], 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(r["per_step"] * 1e3, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "Lq": w.Lq, "Lk": w.Lk, "d": w.d,
+                   "mask": {0: "none", 1: "causal", 2: "key_padding", 3: "causal+key_padding"}[w.mask],
+                   "flops_per_step": w.flops(r["lens"]), "l2": r["l2"],
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "pct_bf16_peak_nominal": round(100.0 * ach / NOMINAL_BF16_TFLOPS, 2),
+        "roofline": {"bound": "tensor", "achieved": round(ach, 2), "peak": peak,
+                     "unit": "TFLOP/s", "frac": round(ach / peak, 4),
+                     "peak_source": f"{peak_src} bf16 burst", "traffic": args.traffic,
+                     "kernel": f"sdpa_fwd_bf16_kernel<{w.d},{2 if w.Lq > 128 else 1},{2 if w.d == 128 else 3}>"},
+        "e2e": r["e2e"],
+        "gpu_launches": args.steps,
+        "clocks": r["clocks"],
+        "cpu_baseline": cpu,
+        "mha_layer": mha_layer,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------------ reference arm
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    from transformer_head_scaled_03_gb300.inputs import WORKLOADS, sample_rows, sdpa_inputs
+
+    w = WORKLOADS[args.workload]
+    Q, K, V, lens, _ = sdpa_inputs(w)
+    rows = sample_rows(w.B, w.H, w.Lq, args.ref_rows_per_head, seed=w.seed + 4000, must=())
+    for _ in range(args.warmup):
+        oracle_cpu_baseline(w, Q, K, V, lens, rows[: max(1, rows.size // 8)])
+    total_s, total_flops = 0.0, 0.0
+    cores = 1
+    for _ in range(args.steps):
+        tf, dt, cores = oracle_cpu_baseline(w, Q, K, V, lens, rows)
+        total_s += dt
+        total_flops += tf * 1e12 * dt
+    value = total_flops / total_s / 1e12
+    sample = (f"{rows.size} query rows per step ({args.ref_rows_per_head} per head, all "
+              f"{w.B * w.H} heads, seeded) of the workload, fp64 oracle")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(total_s / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "Lq": w.Lq, "Lk": w.Lk, "d": w.d},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--workload", type=int, default=5, choices=[2, 3, 4, 5])
+    ap.add_argument("--skip-mha", action="store_true")
+    ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--cpu-rows-per-head", type=int, default=32)
+    ap.add_argument("--ref-rows-per-head", type=int, default=4)
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="DRAM bytes per launch of the fused kernel from an ncu capture")
+    args = ap.parse_args(argv)
+    args.warmup = max(3, args.warmup)   # at least three untimed warm-up steps
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,152 @@
+/*
+ * mha.h -- C ABI of the GB300 (sm_103a) multi-head scaled dot-product
+ * attention library (libmha_gb300.so).
+ *
+ * What the library computes
+ *   Attention(Q, K, V) = softmax(Q K^T * scale + M) V  per (batch, head),
+ *   with scale = 1/sqrt(d_k) by default and M an additive 0/-inf mask
+ *     -- "How Transformers Work" (worksonmygpu.com), "Scaled dot-product
+ *        attention"; "The Transformer" (hoshank.vercel.app), "The
+ *        Mathematics"; masks: "The Transformer" (rayaq.ca), "Masks: who may
+ *        look at whom".
+ *   MultiHead(x_q, x_kv) = Concat(head_1..head_h) W^O,
+ *   head_i = Attention(x_q W^Q_i, x_kv W^K_i, x_kv W^V_i)
+ *     -- hoshank.vercel.app, "The Mathematics" (multi-head equation);
+ *        "32 Transformer" (ml-canon-en), "PyTorch Implementation": y = x @ W,
+ *        head i = column block i of the projection, heads concatenated in
+ *        order before W^O.  No bias terms.
+ *
+ * Conventions shared by every entry point
+ *   - Tensors are dense, row-major (C order), in device memory unless stated
+ *     otherwise, and owned by the caller.  Every tensor pointer must be
+ *     16-byte aligned (TMA requirement); pointers to distinct tensors must
+ *     not overlap, except x_kv == x_q (self-attention).
+ *   - Element type: MHA_BF16 = bfloat16 (uint16 bit pattern), MHA_F32 = IEEE
+ *     float.  bf16 work accumulates in fp32.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *     default stream).  Arguments are validated on the host before anything
+ *     is launched; a call that returns an error has launched nothing.
+ *   - Errors are returned, never printed; the library never aborts.
+ *   - Device-side conditions (a key length outside [1, Lk], a pipeline wait
+ *     that exceeded its time limit) set a per-device error word that
+ *     mha_check() reads.  The affected rows are written as zeros.
+ *   - Masks: mask_kind is a bit set of MHA_MASK_CAUSAL (key j blocked for
+ *     query i when j > i; requires Lq == Lk) and MHA_MASK_KEY_PADDING (key j
+ *     blocked for batch item b when j >= key_lengths[b]).  There are no
+ *     boolean mask tensors, so no mask polarity to get wrong.
+ */
+#ifndef GB300_MHA_H
+#define GB300_MHA_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MHA_OK = 0,
+    MHA_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad size, bad mask */
+    MHA_ERR_UNSUPPORTED = 2, /* valid request outside what is implemented */
+    MHA_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed */
+    MHA_ERR_OOM = 4,         /* device allocation failed (mha_create) */
+    MHA_ERR_TIMEOUT = 5,     /* a kernel pipeline wait gave up (mha_check) */
+    MHA_ERR_DEVICE = 6       /* device-side argument error, e.g. a key
+                                length outside [1, Lk] (mha_check) */
+} mha_status;
+
+typedef enum { MHA_F32 = 0, MHA_BF16 = 1 } mha_dtype;
+
+enum {
+    MHA_MASK_NONE = 0,
+    MHA_MASK_CAUSAL = 1,
+    MHA_MASK_KEY_PADDING = 2
+};
+
+/* Same type as cudaStream_t, declared here so the header needs no CUDA
+ * include. */
+typedef struct CUstream_st *mha_stream;
+
+/* Opaque layer handle: owns the Q/K/V/context workspace for one d_model and
+ * element type. */
+typedef struct mha_ctx *mha_handle;
+
+/*
+ * sdpa_forward -- scaled dot-product attention for B*H independent heads.
+ *   Q [B, H, Lq, d], K [B, H, Lk, d], V [B, H, Lk, d]  (in_dtype)
+ *   O [B, H, Lq, d]                                    (out_dtype)
+ *   scale       : multiplier of Q K^T; 0 selects 1/sqrt(d); must be finite
+ *                 and >= 0.
+ *   mask_kind   : bit set of MHA_MASK_*; CAUSAL requires Lq == Lk.
+ *   key_lengths : device int32[B], required iff KEY_PADDING is set; each
+ *                 value must lie in [1, Lk] (checked on the device).
+ * Supported: in_dtype BF16 with d in {64, 128} (tcgen05 tensor-core path,
+ * out_dtype BF16 or F32); in_dtype F32 with 1 <= d <= 128 (fp32 CUDA-core
+ * path, out_dtype F32).  B, H, Lq may be 0 (nothing is launched); Lk >= 1.
+ * Returns MHA_OK, MHA_ERR_INVALID_ARG, MHA_ERR_UNSUPPORTED or MHA_ERR_CUDA.
+ */
+mha_status sdpa_forward(const void *Q, const void *K, const void *V, void *O,
+                        int B, int H, int Lq, int Lk, int d, float scale,
+                        int mask_kind, const int32_t *key_lengths,
+                        mha_dtype in_dtype, mha_dtype out_dtype,
+                        mha_stream stream);
+
+/*
+ * mha_create -- allocate a multi-head attention layer handle.
+ *   d_model   : model width D.
+ *   dtype     : element type of x, W and out (MHA_BF16 or MHA_F32).
+ *   max_batch, max_lq, max_lk : the largest B, Lq, Lk later calls may use;
+ *               they size the device workspace the handle owns
+ *               (Q [B,H,Lq,d], K and V [B,H,Lk,d], context [B,Lq,D]).
+ * The handle allocates that workspace with cudaMalloc on the current device
+ * and frees it in mha_destroy.  *out is set to NULL on failure.
+ * Returns MHA_OK, MHA_ERR_INVALID_ARG, MHA_ERR_OOM or MHA_ERR_CUDA.
+ */
+mha_status mha_create(mha_handle *out, int d_model, mha_dtype dtype,
+                      int max_batch, int max_lq, int max_lk);
+
+/*
+ * mha_forward -- one multi-head attention layer forward.
+ *   x_q  [B, Lq, D], x_kv [B, Lk, D] (x_kv may equal x_q: self-attention;
+ *        a different tensor: cross-attention, keys/values from x_kv)
+ *   Wq, Wk, Wv, Wo [D, D] row-major, applied as y = x @ W
+ *   h    : number of heads; D % h must be 0; d = D / h.
+ *   mask_kind, key_lengths : as for sdpa_forward.
+ *   out  [B, Lq, D]
+ * The projections write Q, K, V in [B, h, L, d] (the head split is the
+ * store layout); attention writes the context in [B, Lq, D] (the concat is
+ * the store layout); the output projection reads it.  Four launches on
+ * `stream`.  Supported: BF16 with d in {64, 128}; F32 with d <= 128.
+ * Returns MHA_OK, MHA_ERR_INVALID_ARG (incl. B/Lq/Lk above the handle's
+ * maxima), MHA_ERR_UNSUPPORTED or MHA_ERR_CUDA.
+ */
+mha_status mha_forward(mha_handle handle, const void *x_q, const void *x_kv,
+                       const void *Wq, const void *Wk, const void *Wv,
+                       const void *Wo, int B, int Lq, int Lk, int h,
+                       int mask_kind, const int32_t *key_lengths, void *out,
+                       mha_stream stream);
+
+/*
+ * mha_check -- synchronise the current device and report (then clear) its
+ * device-side error word.  `handle` may be NULL.  Returns MHA_OK,
+ * MHA_ERR_TIMEOUT, MHA_ERR_DEVICE or MHA_ERR_CUDA.
+ */
+mha_status mha_check(mha_handle handle);
+
+/* mha_destroy -- free the handle and its workspace (synchronises the
+ * device first).  NULL is accepted. */
+mha_status mha_destroy(mha_handle handle);
+
+/* Static, NUL-terminated name of a status code. */
+const char *mha_status_string(mha_status status);
+
+/* Set the time limit, in milliseconds, after which a kernel pipeline wait
+ * gives up and reports MHA_ERR_TIMEOUT (default 2000; applies to later
+ * launches).  Returns the previous value. */
+int mha_set_wait_limit_ms(int ms);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GB300_MHA_H */

@@ -1,0 +1,226 @@
+"""ctypes binding of libmha_gb300.so (include/mha.h).
+
+Argument marshalling only: tensors become device pointers, the current torch
+stream becomes the cudaStream_t, and status codes become exceptions.  Every
+step of the computation runs in the library's CUDA kernels; there is no CPU
+or PyTorch fallback, and a missing library is an error.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+MHA_OK = 0
+MHA_ERR_INVALID_ARG = 1
+MHA_ERR_UNSUPPORTED = 2
+MHA_ERR_CUDA = 3
+MHA_ERR_OOM = 4
+MHA_ERR_TIMEOUT = 5
+MHA_ERR_DEVICE = 6
+
+MHA_F32 = 0
+MHA_BF16 = 1
+
+MASK_NONE = 0
+MASK_CAUSAL = 1
+MASK_KEY_PADDING = 2
+
+LIB_PATH = _build.LIB
+
+_lock = threading.Lock()
+_lib = None
+
+
+class MhaError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)}")
+
+
+def _declare(lib):
+    vp, i32, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    lib.sdpa_forward.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, i32, vp,
+                                 i32, i32, vp]
+    lib.sdpa_forward.restype = i32
+    lib.mha_create.argtypes = [ctypes.POINTER(vp), i32, i32, i32, i32, i32]
+    lib.mha_create.restype = i32
+    lib.mha_forward.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp]
+    lib.mha_forward.restype = i32
+    lib.mha_check.argtypes = [vp]
+    lib.mha_check.restype = i32
+    lib.mha_destroy.argtypes = [vp]
+    lib.mha_destroy.restype = i32
+    lib.mha_status_string.argtypes = [i32]
+    lib.mha_status_string.restype = ctypes.c_char_p
+    lib.mha_set_wait_limit_ms.argtypes = [i32]
+    lib.mha_set_wait_limit_ms.restype = i32
+    return lib
+
+
+def lib():
+    """The loaded library.  Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"CUDA library {LIB_PATH} is missing; build it with "
+                    "transformer_head_scaled_03_gb300.build.build()")
+            _lib = _declare(ctypes.CDLL(LIB_PATH))
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().mha_status_string(int(status)).decode()
+
+
+def _check(status: int, what: str):
+    if status != MHA_OK:
+        raise MhaError(status, what)
+
+
+def _dtype_code(t: torch.dtype) -> int:
+    if t == torch.bfloat16:
+        return MHA_BF16
+    if t == torch.float32:
+        return MHA_F32
+    raise TypeError(f"unsupported dtype {t}")
+
+
+def _dev_ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("tensor must be on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError("tensor must be contiguous")
+    return ctypes.c_void_p(t.data_ptr()) if t.numel() else None
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def sdpa_forward(Q, K, V, scale: float | None = None, mask_kind: int = MASK_NONE,
+                 key_lengths=None, out_dtype: torch.dtype | None = None, out=None,
+                 stream=None):
+    """O = softmax(Q K^T * scale + mask) V for Q [B,H,Lq,d], K/V [B,H,Lk,d]."""
+    B, H, Lq, d = Q.shape
+    Lk = K.shape[2]
+    if K.shape != (B, H, Lk, d) or V.shape != (B, H, Lk, d):
+        raise ValueError("Q/K/V shapes disagree")
+    if K.dtype != Q.dtype or V.dtype != Q.dtype:
+        raise ValueError("Q/K/V dtypes disagree")
+    odt = out_dtype or Q.dtype
+    if out is None:
+        out = torch.empty((B, H, Lq, d), dtype=odt, device=Q.device)
+    elif out.shape != (B, H, Lq, d) or out.dtype != odt:
+        raise ValueError("out has the wrong shape or dtype")
+    if key_lengths is not None and key_lengths.dtype != torch.int32:
+        raise ValueError("key_lengths must be int32")
+    st = lib().sdpa_forward(_dev_ptr(Q), _dev_ptr(K), _dev_ptr(V), _dev_ptr(out), B, H, Lq, Lk,
+                            d, float(scale or 0.0), int(mask_kind), _dev_ptr(key_lengths),
+                            _dtype_code(Q.dtype), _dtype_code(odt), _stream(stream))
+    _check(st, "sdpa_forward")
+    return out
+
+
+class MhaHandle:
+    """Owner of an ``mha_create`` handle (destroyed with ``close``)."""
+
+    def __init__(self, d_model: int, dtype: torch.dtype, max_batch: int, max_lq: int,
+                 max_lk: int):
+        h = ctypes.c_void_p()
+        _check(lib().mha_create(ctypes.byref(h), d_model, _dtype_code(dtype), max_batch, max_lq,
+                                max_lk), "mha_create")
+        self._h = h
+        self.d_model, self.dtype = d_model, dtype
+
+    @property
+    def raw(self):
+        if self._h is None:
+            raise RuntimeError("handle destroyed")
+        return self._h
+
+    def close(self):
+        if self._h is not None:
+            _check(lib().mha_destroy(self._h), "mha_destroy")
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def mha_create(d_model: int, dtype: torch.dtype, max_batch: int, max_lq: int,
+               max_lk: int) -> MhaHandle:
+    return MhaHandle(d_model, dtype, max_batch, max_lq, max_lk)
+
+
+def mha_forward(handle: MhaHandle, x_q, x_kv, Wq, Wk, Wv, Wo, h: int,
+                mask_kind: int = MASK_NONE, key_lengths=None, out=None, stream=None):
+    """out = Concat(head_1..head_h) Wo, head_i = Attention(x_q Wq_i, x_kv Wk_i, x_kv Wv_i)."""
+    B, Lq, D = x_q.shape
+    Lk = x_kv.shape[1]
+    if x_kv.shape != (B, Lk, D):
+        raise ValueError("x_kv shape")
+    for W in (Wq, Wk, Wv, Wo):
+        if W.shape != (D, D) or W.dtype != x_q.dtype:
+            raise ValueError("weights must be [D, D] of the activations' dtype")
+    if out is None:
+        out = torch.empty((B, Lq, D), dtype=x_q.dtype, device=x_q.device)
+    st = lib().mha_forward(handle.raw, _dev_ptr(x_q), _dev_ptr(x_kv), _dev_ptr(Wq),
+                           _dev_ptr(Wk), _dev_ptr(Wv), _dev_ptr(Wo), B, Lq, Lk, int(h),
+                           int(mask_kind), _dev_ptr(key_lengths), _dev_ptr(out),
+                           _stream(stream))
+    _check(st, "mha_forward")
+    return out
+
+
+def mha_check(handle: MhaHandle | None = None) -> int:
+    """Synchronise and return (then clear) the device error status code."""
+    return int(lib().mha_check(handle.raw if handle is not None else None))
+
+
+def mha_destroy(handle: MhaHandle):
+    handle.close()
+
+
+def set_wait_limit_ms(ms: int) -> int:
+    return int(lib().mha_set_wait_limit_ms(int(ms)))
+
+
+def sdpa_forward_host(Qh, Kh, Vh, scale=None, mask_kind=MASK_NONE, lengths_h=None,
+                      out_dtype=None, device="cuda", bufs=None):
+    """End-to-end call from host (pinned) tensors: copy in, attend, copy out.
+
+    ``bufs`` (a dict) keeps device and pinned buffers between calls."""
+    bufs = {} if bufs is None else bufs
+
+    def dev(name, src):
+        t = bufs.get(name)
+        if t is None or t.shape != src.shape or t.dtype != src.dtype:
+            t = bufs[name] = torch.empty(src.shape, dtype=src.dtype, device=device)
+        t.copy_(src, non_blocking=True)
+        return t
+
+    Q, K, V = dev("Q", Qh), dev("K", Kh), dev("V", Vh)
+    kl = dev("len", lengths_h) if lengths_h is not None else None
+    odt = out_dtype or Qh.dtype
+    O = bufs.get("O")
+    if O is None or O.shape != Q.shape or O.dtype != odt:
+        O = bufs["O"] = torch.empty(Q.shape, dtype=odt, device=device)
+    sdpa_forward(Q, K, V, scale=scale, mask_kind=mask_kind, key_lengths=kl, out=O)
+    Oh = bufs.get("Oh")
+    if Oh is None or Oh.shape != O.shape or Oh.dtype != odt:
+        Oh = bufs["Oh"] = torch.empty(O.shape, dtype=odt, pin_memory=True)
+    Oh.copy_(O, non_blocking=True)
+    return Oh

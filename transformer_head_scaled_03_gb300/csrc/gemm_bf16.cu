@@ -1,0 +1,239 @@
+// gemm_bf16.cu -- the Q/K/V/O projections, C = A @ W (bf16 in, fp32
+// accumulate in tensor memory, bf16 out), on sm_103a tcgen05 tensor cores.
+//
+// y = x @ W with W stored [d_in, d_out] ("32 Transformer" (ml-canon-en),
+// "PyTorch Implementation"; "The Transformer" (hoshank.vercel.app), the
+// multi-head equation).  The head split is folded into the store: column n
+// of the projection belongs to head n / d and lands in the [B, H, L, d]
+// tensor the attention kernel reads.  The output projection reads the
+// concatenated heads [B, Lq, H*d] that the attention kernel writes, so the
+// concat is a store layout too, never a copy.
+//
+// CTA tile 128 x 256, k-step 64, a 4-stage TMA ring.  A (activations) is
+// K-major; W is row-major [K, N], i.e. MN-major for the MMA's B operand, and
+// is loaded as 64 x 64 boxes (64 N-columns of 128 bytes, 64 K-rows).
+// Warp roles: warp 0 TMA producer, warp 1 MMA issuer and TMEM owner,
+// warps 2-5 epilogue (TMEM -> registers -> global, one row per thread).
+// Up to three problems of one shape share a launch (grid.z), which is how
+// the Q, K and V projections of self-attention run as one launch.
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace mha {
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kBN = 256;
+constexpr int kBK = 64;
+constexpr int kStages = 4;
+constexpr int kABytes = kBM * kBK * 2;           // 16 KB
+constexpr int kWBox = 64 * 64 * 2;               // 8 KB: one 64(N) x 64(K) box
+constexpr int kWBytes = kBK * kBN * 2;           // 32 KB
+constexpr int kStageBytes = kABytes + kWBytes;   // 48 KB
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 256;
+// barriers: full[kStages], empty[kStages], acc_full, drain
+__host__ __device__ constexpr int bFull(int s) { return s; }
+__host__ __device__ constexpr int bEmpty(int s) { return kStages + s; }
+constexpr int bAcc = 2 * kStages;
+constexpr int bDrain = 2 * kStages + 1;
+constexpr int kNumBars = 2 * kStages + 2;
+constexpr int kOffBar = kStages * kStageBytes;
+constexpr int kOffMisc = kOffBar + 8 * kNumBars;
+constexpr int kSmemBytes = kOffMisc + 16 + 1024;
+static_assert(kSmemBytes <= 232448, "shared memory");
+
+struct GemmParams {
+  void* C[3];
+  int store[3];
+  int L[3];
+  int dh[3];
+  int M, N, K;
+  unsigned* err;
+  uint64_t limit_ns;
+};
+
+__device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_timer_ns() - t0 > limit_ns) return;
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_bf16_kernel(const __grid_constant__ CUtensorMap tA0, const __grid_constant__ CUtensorMap tA1,
+                     const __grid_constant__ CUtensorMap tA2, const __grid_constant__ CUtensorMap tW0,
+                     const __grid_constant__ CUtensorMap tW1, const __grid_constant__ CUtensorMap tW2,
+                     const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + kOffMisc);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + kOffMisc + 4);
+  auto bar = [base](int i) -> uint32_t { return base + kOffBar + 8u * i; };
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const WaitCtl ctl{abort_flag, p.err, p.limit_ns};
+  const int z = blockIdx.z;
+  const CUtensorMap* tA = z == 0 ? &tA0 : (z == 1 ? &tA1 : &tA2);
+  const CUtensorMap* tW = z == 0 ? &tW0 : (z == 1 ? &tW1 : &tW2);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(bar(bFull(s)), 1);
+      mbar_init(bar(bEmpty(s)), 1);
+    }
+    mbar_init(bar(bAcc), 1);
+    mbar_init(bar(bDrain), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc<kTmemCols>(smem_u32(tmem_slot));
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(tA);
+    tma_prefetch_desc(tW);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+
+  const int n0 = blockIdx.x * kBN;
+  const int m0 = blockIdx.y * kBM;
+  const int num_k = (p.K + kBK - 1) / kBK;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int issued = 0;
+      for (int kt = 0; kt < num_k; ++kt) {
+        const int st = kt % kStages;
+        const uint32_t ph = (kt / kStages) & 1;
+        if (!mbar_wait(bar(bEmpty(st)), ph ^ 1u, ctl)) break;
+        const uint32_t sa = base + st * kStageBytes;
+        mbar_expect_tx(bar(bFull(st)), kStageBytes);
+        tma_load_2d(sa, tA, bar(bFull(st)), kt * kBK, m0);
+#pragma unroll
+        for (int nb = 0; nb < kBN / 64; ++nb)
+          tma_load_2d(sa + kABytes + nb * kWBox, tW, bar(bFull(st)), n0 + nb * 64, kt * kBK);
+        issued = kt + 1;
+      }
+      for (int kt = max(0, issued - kStages); kt < issued; ++kt)
+        wait_drain(bar(bFull(kt % kStages)), (kt / kStages) & 1, p.limit_ns);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, kBN, false, true);
+      bool ok = true;
+      for (int kt = 0; kt < num_k; ++kt) {
+        const int st = kt % kStages;
+        const uint32_t ph = (kt / kStages) & 1;
+        if (!(ok = mbar_wait(bar(bFull(st)), ph, ctl))) break;
+        tc_fence_after();
+        const uint32_t sa = base + st * kStageBytes;
+        const uint32_t sw = sa + kABytes;
+#pragma unroll
+        for (int ks = 0; ks < kBK / 16; ++ks) {
+          // A: K-major, +32 bytes per 16 k; W: MN-major, +16 rows of 128 bytes
+          umma_ss(tmem, sdesc_sw128(sa + ks * 32, 16, 1024),
+                  sdesc_sw128(sw + ks * 16 * 128, kWBox, 1024), kIdesc,
+                  (kt > 0 || ks > 0) ? 1u : 0u);
+        }
+        umma_commit(bar(bEmpty(st)));
+      }
+      if (ok) umma_commit(bar(bAcc));
+      umma_commit(bar(bDrain));
+      wait_drain(bar(bDrain), 0, p.limit_ns);
+    }
+  } else {
+    // epilogue: warp w may read TMEM lanes [32*(w%4), 32*(w%4)+32)
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const int m = m0 + row;
+    const bool ok = num_k > 0 && mbar_wait_warp(bar(bAcc), 0, ctl);
+    if (ok) tc_fence_after();
+    const int store = p.store[z];
+    const int L = p.L[z], dh = p.dh[z];
+    __nv_bfloat16* C = static_cast<__nv_bfloat16*>(p.C[z]);
+    const uint32_t tbase = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    for (int cb = 0; cb < kBN / 32; ++cb) {
+      const int n = n0 + cb * 32;
+      if (n >= p.N) break;  // uniform across the warp
+      uint32_t v[32];
+      if (ok) {
+        tmem_ld32(tbase + cb * 32, v);
+        tmem_ld_wait(v);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = 0u;
+      }
+      if (m < p.M) {
+        size_t off;
+        if (store == static_cast<int>(GemmStore::kHeadSplit)) {
+          const int bb = m / L, l = m - bb * L, hh = n / dh, c = n - hh * dh;
+          off = ((static_cast<size_t>(bb) * (p.N / dh) + hh) * L + l) * dh + c;
+        } else {
+          off = static_cast<size_t>(m) * p.N + n;
+        }
+        uint4* dst = reinterpret_cast<uint4*>(C + off);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          uint4 w;
+          w.x = pack_bf16x2(__uint_as_float(v[8 * i + 0]), __uint_as_float(v[8 * i + 1]));
+          w.y = pack_bf16x2(__uint_as_float(v[8 * i + 2]), __uint_as_float(v[8 * i + 3]));
+          w.z = pack_bf16x2(__uint_as_float(v[8 * i + 4]), __uint_as_float(v[8 * i + 5]));
+          w.w = pack_bf16x2(__uint_as_float(v[8 * i + 6]), __uint_as_float(v[8 * i + 7]));
+          dst[i] = w;
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc<kTmemCols>(tmem);
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_bf16(const GemmArgs& g, const DeviceCtl& ctl) {
+  if (g.M == 0 || g.N == 0) return cudaSuccess;
+  CUtensorMap ta[3], tw[3];
+  GemmParams p{};
+  for (int i = 0; i < 3; ++i) {
+    const GemmProblem& pr = g.prob[i < g.count ? i : 0];
+    const uint64_t adims[2] = {static_cast<uint64_t>(g.K), static_cast<uint64_t>(g.M)};
+    const uint64_t astr[1] = {static_cast<uint64_t>(g.K) * 2};
+    const uint32_t abox[2] = {64, 128};
+    const uint64_t wdims[2] = {static_cast<uint64_t>(g.N), static_cast<uint64_t>(g.K)};
+    const uint64_t wstr[1] = {static_cast<uint64_t>(g.N) * 2};
+    const uint32_t wbox[2] = {64, 64};
+    if (!encode_tensor_map(&ta[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(pr.A),
+                           adims, astr, abox, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tensor_map(&tw[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(pr.W),
+                           wdims, wstr, wbox, CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+    p.C[i] = pr.C;
+    p.store[i] = static_cast<int>(pr.store);
+    p.L[i] = pr.L > 0 ? pr.L : 1;
+    p.dh[i] = pr.dh > 0 ? pr.dh : 1;
+  }
+  p.M = g.M;
+  p.N = g.N;
+  p.K = g.K;
+  p.err = ctl.err;
+  p.limit_ns = ctl.limit_ns;
+  cudaError_t e = cudaFuncSetAttribute(gemm_bf16_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const dim3 grid((g.N + kBN - 1) / kBN, (g.M + kBM - 1) / kBM, g.count);
+  gemm_bf16_kernel<<<grid, kThreads, kSmemBytes, g.stream>>>(ta[0], ta[1], ta[2], tw[0], tw[1],
+                                                              tw[2], p);
+  return cudaGetLastError();
+}
+
+}  // namespace mha

@@ -1,0 +1,66 @@
+// internal.h -- declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "mha.h"
+
+namespace mha {
+
+// One scaled dot-product attention launch.
+struct SdpaArgs {
+  const void* Q;  // [B, H, Lq, d]
+  const void* K;  // [B, H, Lk, d]
+  const void* V;  // [B, H, Lk, d]
+  void* O;        // [B, H, Lq, d], or [B, Lq, H*d] when ctx_layout
+  int B, H, Lq, Lk, d;
+  float scale;  // resolved (> 0)
+  int mask_kind;
+  const int32_t* key_lengths;  // device, or nullptr
+  mha_dtype in_dtype, out_dtype;
+  bool ctx_layout;
+  cudaStream_t stream;
+};
+
+// Row-major GEMM C = A[M,K] @ W[K,N] with a choice of store layout.
+enum class GemmStore : int {
+  kRowMajor = 0,   // C[m, n] at m*N + n
+  kHeadSplit = 1,  // m = b*L + l, n = h*dh + c  ->  C[b, h, l, c]
+};
+
+struct GemmProblem {
+  const void* A;  // [M, K]
+  const void* W;  // [K, N]
+  void* C;
+  GemmStore store;
+  int L;   // rows per batch item (head split)
+  int dh;  // head width (head split)
+};
+
+struct GemmArgs {
+  GemmProblem prob[3];  // up to three problems with one shape, one launch
+  int count;
+  int M, N, K;
+  mha_dtype dtype;
+  cudaStream_t stream;
+};
+
+struct DeviceCtl {
+  unsigned* err;       // device error word
+  uint64_t limit_ns;   // wait limit for pipelined kernels
+};
+
+cudaError_t launch_sdpa_bf16(const SdpaArgs& a, const DeviceCtl& ctl);
+cudaError_t launch_sdpa_f32(const SdpaArgs& a, const DeviceCtl& ctl);
+cudaError_t launch_gemm_bf16(const GemmArgs& g, const DeviceCtl& ctl);
+cudaError_t launch_gemm_f32(const GemmArgs& g, const DeviceCtl& ctl);
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point.
+// Returns false when the entry point is unavailable or encoding failed.
+bool encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t rank,
+                       void* base, const uint64_t* dims, const uint64_t* strides_bytes,
+                       const uint32_t* box, CUtensorMapSwizzle swizzle);
+
+}  // namespace mha

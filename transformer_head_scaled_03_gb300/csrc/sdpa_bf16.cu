@@ -1,0 +1,439 @@
+// sdpa_bf16.cu -- fused scaled dot-product attention forward, bf16 in, fp32
+// accumulate, for sm_103a (tcgen05 tensor cores, tensor memory, TMA).
+//
+// Computes, per (batch b, head h) and query row i,
+//     O[i] = sum_j softmax_j(scale * <Q[i], K[j]> + M[i][j]) V[j]
+// ("How Transformers Work" (worksonmygpu.com), "Scaled dot-product
+// attention"; masks as in "The Transformer" (rayaq.ca), "Masks: who may look
+// at whom") without ever writing the Lq x Lk score matrix to memory: keys
+// are visited in 128-key tiles and the softmax is accumulated online (a
+// running row maximum m and row sum l in fp32; when m grows the partial
+// output is rescaled by 2^((m_old - m_new) * scale * log2 e)).  This is the
+// exact-attention-by-tiling idea the pages credit to FlashAttention
+// ("32 Transformer" (ml-canon-en), "Connections"), laid out for tcgen05.
+//
+// CTA = NQT query tiles of 128 rows of one (b, h).  Warp roles:
+//   warps 0 .. 4*NQT-1 : one softmax warpgroup per query tile; thread r of
+//                        the group owns query row r (TMEM lane r), so the
+//                        row max and row sum are thread-local.
+//   warp 4*NQT         : TMA producer (Q once, then a ring of NST K and V
+//                        stages, 128-byte swizzled).
+//   warp 4*NQT+1       : MMA issuer (one thread) and TMEM owner.
+// Per key tile j and query tile t:
+//   S_t  = Q_t K_j^T           tcgen05.mma, A and B from shared memory,
+//                              fp32 accumulator in TMEM (128 columns)
+//   P_t  = 2^(S_t*c - m*c)     softmax warps: tcgen05.ld of S, mask, online
+//                              max/sum, P packed to bf16 and tcgen05.st back
+//                              into the first 64 columns of S_t
+//   O_t += P_t V_j             tcgen05.mma with A = P_t from TMEM and
+//                              B = V_j (MN-major) from shared memory
+// The epilogue divides O_t by l and stores bf16 or fp32, either as
+// [B,H,Lq,d] or directly in the concatenated-heads layout [B,Lq,H*d].
+#include <math.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace mha {
+namespace {
+
+constexpr int kBlockM = 128;      // query rows per tile = TMEM lanes
+constexpr int kBlockN = 128;      // keys per K/V tile
+constexpr int kSub = 128 * 128;   // bytes of a 128-row x 64-column bf16 block
+
+struct SdpaParams {
+  void* O;
+  const int32_t* key_lengths;
+  unsigned* err;
+  uint64_t limit_ns;
+  int B, H, Lq, Lk;
+  int num_q_blocks;
+  int mask_kind;
+  float scale_log2;  // scale * log2(e)
+  int out_f32;
+  int ctx_layout;
+};
+
+template <int D, int NQT, int NST>
+struct Cfg {
+  static_assert(D == 64 || D == 128, "head dim");
+  static constexpr int KB = D / 64;               // 64-column (128-byte) blocks per row
+  static constexpr int kTileBytes = KB * kSub;    // one 128-row tile of Q, K or V
+  static constexpr int kSoftmaxWarps = 4 * NQT;
+  static constexpr int kTmaWarp = kSoftmaxWarps;
+  static constexpr int kMmaWarp = kSoftmaxWarps + 1;
+  static constexpr int kThreads = 32 * (kSoftmaxWarps + 2);
+  static constexpr int kTmemNeed = NQT * (kBlockN + D);
+  static constexpr uint32_t kTmemCols = kTmemNeed <= 256 ? 256u : 512u;
+  static_assert(kTmemNeed <= 512, "TMEM budget");
+  // tensor-memory columns
+  __host__ __device__ static constexpr uint32_t tS(int t) { return static_cast<uint32_t>(t * kBlockN); }
+  __host__ __device__ static constexpr uint32_t tO(int t) { return static_cast<uint32_t>(NQT * kBlockN + t * D); }
+  // barrier indices
+  static constexpr int bQ = 0;
+  __host__ __device__ static constexpr int bKF(int s) { return 1 + s; }
+  __host__ __device__ static constexpr int bKE(int s) { return 1 + NST + s; }
+  __host__ __device__ static constexpr int bVF(int s) { return 1 + 2 * NST + s; }
+  __host__ __device__ static constexpr int bVE(int s) { return 1 + 3 * NST + s; }
+  __host__ __device__ static constexpr int bS(int t) { return 1 + 4 * NST + t; }
+  __host__ __device__ static constexpr int bP(int t) { return 1 + 4 * NST + NQT + t; }
+  __host__ __device__ static constexpr int bO(int t) { return 1 + 4 * NST + 2 * NQT + t; }
+  static constexpr int bDrain = 1 + 4 * NST + 3 * NQT;
+  static constexpr int kNumBars = bDrain + 1;
+  // shared-memory layout from a 1024-byte aligned base
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = kOffQ + NQT * kTileBytes;
+  static constexpr int kOffV = kOffK + NST * kTileBytes;
+  static constexpr int kOffBar = kOffV + NST * kTileBytes;
+  static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
+  static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
+  static_assert(kSmemBytes <= 232448, "shared memory");
+};
+
+// Bounded wait that ignores the abort flag: used to let copies and MMAs that
+// are already in flight land before the CTA releases its memory.
+__device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_timer_ns() - t0 > limit_ns) return;
+  }
+}
+
+template <int D, int NQT, int NST>
+__global__ void __launch_bounds__(Cfg<D, NQT, NST>::kThreads, 1)
+    sdpa_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ,
+                         const __grid_constant__ CUtensorMap tmK,
+                         const __grid_constant__ CUtensorMap tmV, const SdpaParams p) {
+  using C = Cfg<D, NQT, NST>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + C::kOffMisc);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kOffMisc + 4);
+  auto bar = [base](int i) -> uint32_t { return base + C::kOffBar + 8u * i; };
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const WaitCtl ctl{abort_flag, p.err, p.limit_ns};
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(C::bQ), 1);
+    for (int s = 0; s < NST; ++s) {
+      mbar_init(bar(C::bKF(s)), 1);
+      mbar_init(bar(C::bKE(s)), 1);
+      mbar_init(bar(C::bVF(s)), 1);
+      mbar_init(bar(C::bVE(s)), 1);
+    }
+    for (int t = 0; t < NQT; ++t) {
+      mbar_init(bar(C::bS(t)), 1);
+      mbar_init(bar(C::bP(t)), kBlockM);
+      mbar_init(bar(C::bO(t)), 1);
+    }
+    mbar_init(bar(C::bDrain), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == C::kMmaWarp) {
+    tmem_alloc<C::kTmemCols>(smem_u32(tmem_slot));
+    tmem_relinquish();
+  }
+  if (warp == C::kTmaWarp && lane == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+
+  // ---- which (b, h, query block) this CTA computes; causal blocks are
+  // visited longest-first so the short ones fill the tail of the grid.
+  const int BH = p.B * p.H;
+  const bool causal = (p.mask_kind & MHA_MASK_CAUSAL) != 0;
+  const bool padded = (p.mask_kind & MHA_MASK_KEY_PADDING) != 0;
+  const int blk = static_cast<int>(blockIdx.x) / BH;
+  const int bh = static_cast<int>(blockIdx.x) - blk * BH;
+  const int qb = causal ? (p.num_q_blocks - 1 - blk) : blk;
+  const int b = bh / p.H;
+  const int h = bh - b * p.H;
+  const int q0 = qb * (NQT * kBlockM);
+  int key_end = p.Lk;  // keys [0, key_end) pass the padding rule
+  bool bad_len = false;
+  if (padded) {
+    const int L = __ldg(p.key_lengths + b);
+    if (L < 1 || L > p.Lk) bad_len = true;
+    else key_end = L;
+  }
+  int kv_stop = bad_len ? 0 : key_end;
+  if (causal) kv_stop = min(kv_stop, q0 + NQT * kBlockM);
+  const int n_kv = (kv_stop + kBlockN - 1) / kBlockN;
+  if (bad_len && threadIdx.x == 0) atomicOr(p.err, kErrKeyLength);
+
+  if (warp == C::kTmaWarp) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0 && n_kv > 0) {
+      mbar_expect_tx(bar(C::bQ), NQT * C::kTileBytes);
+      for (int t = 0; t < NQT; ++t)
+        for (int kb = 0; kb < C::KB; ++kb)
+          tma_load_3d(base + C::kOffQ + (t * C::KB + kb) * kSub, &tmQ, bar(C::bQ), kb * 64,
+                      q0 + t * kBlockM, bh);
+      int k_issued = 0, v_issued = 0;
+      for (int j = 0; j < n_kv; ++j) {
+        const int st = j % NST;
+        const uint32_t ph = (j / NST) & 1;
+        if (!mbar_wait(bar(C::bKE(st)), ph ^ 1u, ctl)) break;
+        mbar_expect_tx(bar(C::bKF(st)), C::kTileBytes);
+        for (int kb = 0; kb < C::KB; ++kb)
+          tma_load_3d(base + C::kOffK + (st * C::KB + kb) * kSub, &tmK, bar(C::bKF(st)),
+                      kb * 64, j * kBlockN, bh);
+        k_issued = j + 1;
+        if (!mbar_wait(bar(C::bVE(st)), ph ^ 1u, ctl)) break;
+        mbar_expect_tx(bar(C::bVF(st)), C::kTileBytes);
+        for (int kb = 0; kb < C::KB; ++kb)
+          tma_load_3d(base + C::kOffV + (st * C::KB + kb) * kSub, &tmV, bar(C::bVF(st)),
+                      kb * 64, j * kBlockN, bh);
+        v_issued = j + 1;
+      }
+      // let every issued copy land before the CTA can exit
+      wait_drain(bar(C::bQ), 0, p.limit_ns);
+      for (int j = max(0, k_issued - NST); j < k_issued; ++j)
+        wait_drain(bar(C::bKF(j % NST)), (j / NST) & 1, p.limit_ns);
+      for (int j = max(0, v_issued - NST); j < v_issued; ++j)
+        wait_drain(bar(C::bVF(j % NST)), (j / NST) & 1, p.limit_ns);
+    }
+  } else if (warp == C::kMmaWarp) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0 && n_kv > 0) {
+      constexpr uint32_t kIdescQK = idesc_bf16_f32(kBlockM, kBlockN, false, false);
+      constexpr uint32_t kIdescPV = idesc_bf16_f32(kBlockM, D, false, true);
+      bool ok = mbar_wait(bar(C::bQ), 0, ctl);
+      for (int j = 0; ok && j < n_kv; ++j) {
+        const int st = j % NST;
+        const uint32_t ph = (j / NST) & 1;
+        if (!(ok = mbar_wait(bar(C::bKF(st)), ph, ctl))) break;
+        tc_fence_after();
+        for (int t = 0; t < NQT && ok; ++t) {
+          // S_t aliases P_t of the previous tile: wait until that P.V is done
+          if (j > 0) {
+            if (!(ok = mbar_wait(bar(C::bO(t)), (j - 1) & 1, ctl))) break;
+            tc_fence_after();
+          }
+          const uint32_t qa = base + C::kOffQ + t * C::kTileBytes;
+          const uint32_t kbase = base + C::kOffK + st * C::kTileBytes;
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks) {
+            const uint32_t off = (ks >> 2) * kSub + (ks & 3) * 32;  // 16 elements = 32 bytes
+            umma_ss(tmem + C::tS(t), sdesc_sw128(qa + off, 16, 1024),
+                    sdesc_sw128(kbase + off, 16, 1024), kIdescQK, ks > 0 ? 1u : 0u);
+          }
+          umma_commit(bar(C::bS(t)));
+        }
+        if (!ok) break;
+        umma_commit(bar(C::bKE(st)));
+        if (!(ok = mbar_wait(bar(C::bVF(st)), ph, ctl))) break;
+        const uint32_t vbase = base + C::kOffV + st * C::kTileBytes;
+        for (int t = 0; t < NQT && ok; ++t) {
+          if (!(ok = mbar_wait(bar(C::bP(t)), j & 1, ctl))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int ks = 0; ks < kBlockN / 16; ++ks) {
+            // 16 keys of V = 16 rows of 128 bytes; P: 16 bf16 = 8 TMEM columns
+            umma_ts(tmem + C::tO(t), tmem + C::tS(t) + ks * 8,
+                    sdesc_sw128(vbase + ks * 16 * 128, kSub, 1024), kIdescPV,
+                    (j > 0 || ks > 0) ? 1u : 0u);
+          }
+          umma_commit(bar(C::bO(t)));
+        }
+        if (!ok) break;
+        umma_commit(bar(C::bVE(st)));
+      }
+      // every issued MMA completes before tensor memory is released
+      umma_commit(bar(C::bDrain));
+      wait_drain(bar(C::bDrain), 0, p.limit_ns);
+    }
+  } else {
+    // --------------------------------------------------- softmax warpgroup
+    const int t = warp >> 2;
+    const int quarter = warp & 3;  // this warp may touch TMEM lanes [32q, 32q+32)
+    const int r = quarter * 32 + lane;
+    const int q_row = q0 + t * kBlockM + r;
+    const uint32_t lane_bits = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t tS = tmem + lane_bits + C::tS(t);
+    const uint32_t tO = tmem + lane_bits + C::tO(t);
+    const float sl2 = p.scale_log2;
+    float m = -INFINITY;  // running max of the raw (unscaled, masked) scores
+    float l = 0.f;        // running sum of 2^((s - m) * sl2)
+    bool ok = true;
+    for (int j = 0; j < n_kv; ++j) {
+      if (!(ok = mbar_wait_warp(bar(C::bS(t)), j & 1, ctl))) break;
+      tc_fence_after();
+      uint32_t s[128];
+      tmem_ld32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
+      tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
+      tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(&s[64]));
+      tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(&s[96]));
+      tmem_ld_wait(s);
+      float x[128];
+#pragma unroll
+      for (int c = 0; c < 128; ++c) x[c] = __uint_as_float(s[c]);
+      const int k0 = j * kBlockN;
+      const bool edge = (k0 + kBlockN > key_end) ||
+                        (causal && k0 + kBlockN - 1 > q0 + t * kBlockM);
+      if (edge) {
+#pragma unroll
+        for (int c = 0; c < 128; ++c) {
+          const int key = k0 + c;
+          if (key >= key_end || (causal && key > q_row)) x[c] = -INFINITY;
+        }
+      }
+      float mt = x[0];
+#pragma unroll
+      for (int c = 1; c < 128; ++c) mt = fmaxf(mt, x[c]);
+      const float m_new = fmaxf(m, mt);
+      const float alpha = (m_new == -INFINITY) ? 1.f : ex2_approx((m - m_new) * sl2);
+      l *= alpha;
+      m = m_new;
+      const float mb = (m == -INFINITY) ? 0.f : m * sl2;
+      float rs = 0.f;
+      uint32_t pk[64];
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        const float p0 = ex2_approx(fmaf(x[2 * c], sl2, -mb));
+        const float p1 = ex2_approx(fmaf(x[2 * c + 1], sl2, -mb));
+        rs += p0 + p1;
+        pk[c] = pack_bf16x2(p0, p1);
+      }
+      l += rs;
+      tmem_st32(tS + 0, *reinterpret_cast<const uint32_t(*)[32]>(&pk[0]));
+      tmem_st32(tS + 32, *reinterpret_cast<const uint32_t(*)[32]>(&pk[32]));
+      // Rescale the partial output when the running max grew.  P.V of the
+      // previous tile is complete: its commit preceded this tile's S commit.
+      // Done after P is stored, when the score registers are free again.
+      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+        for (int cb = 0; cb < D / 32; ++cb) {
+          uint32_t o[32];
+          tmem_ld32(tO + cb * 32, o);
+          tmem_ld_wait(o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st32(tO + cb * 32, o);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(C::bP(t)));
+    }
+    // ------------------------------------------------------------ epilogue
+    bool have = ok && n_kv > 0;
+    if (have) {
+      have = mbar_wait_warp(bar(C::bO(t)), (n_kv - 1) & 1, ctl);
+      tc_fence_after();
+    }
+    const float inv_l = (have && l > 0.f) ? 1.f / l : 0.f;
+    const size_t row_idx = p.ctx_layout
+                               ? (static_cast<size_t>(b) * p.Lq + q_row) * p.H + h
+                               : static_cast<size_t>(bh) * p.Lq + q_row;
+#pragma unroll
+    for (int cb = 0; cb < D / 32; ++cb) {
+      uint32_t o[32];
+      if (have) {
+        tmem_ld32(tO + cb * 32, o);
+        tmem_ld_wait(o);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[i] = 0u;
+      }
+      if (q_row < p.Lq) {
+        if (p.out_f32) {
+          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.O) + row_idx * D + cb * 32);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            dst[i] = make_float4(__uint_as_float(o[4 * i]) * inv_l,
+                                 __uint_as_float(o[4 * i + 1]) * inv_l,
+                                 __uint_as_float(o[4 * i + 2]) * inv_l,
+                                 __uint_as_float(o[4 * i + 3]) * inv_l);
+        } else {
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.O) + row_idx * D +
+                                                cb * 32);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            uint4 v;
+            v.x = pack_bf16x2(__uint_as_float(o[8 * i + 0]) * inv_l,
+                              __uint_as_float(o[8 * i + 1]) * inv_l);
+            v.y = pack_bf16x2(__uint_as_float(o[8 * i + 2]) * inv_l,
+                              __uint_as_float(o[8 * i + 3]) * inv_l);
+            v.z = pack_bf16x2(__uint_as_float(o[8 * i + 4]) * inv_l,
+                              __uint_as_float(o[8 * i + 5]) * inv_l);
+            v.w = pack_bf16x2(__uint_as_float(o[8 * i + 6]) * inv_l,
+                              __uint_as_float(o[8 * i + 7]) * inv_l);
+            dst[i] = v;
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == C::kMmaWarp) tmem_dealloc<C::kTmemCols>(tmem);
+}
+
+template <int D, int NQT, int NST>
+cudaError_t launch_impl(const SdpaArgs& a, const DeviceCtl& ctl) {
+  using C = Cfg<D, NQT, NST>;
+  CUtensorMap maps[3];
+  const void* ptrs[3] = {a.Q, a.K, a.V};
+  const int lens[3] = {a.Lq, a.Lk, a.Lk};
+  for (int i = 0; i < 3; ++i) {
+    const uint64_t dims[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(lens[i]),
+                              static_cast<uint64_t>(a.B) * a.H};
+    const uint64_t strides[2] = {static_cast<uint64_t>(D) * 2,
+                                 static_cast<uint64_t>(lens[i]) * D * 2};
+    const uint32_t box[3] = {64, 128, 1};
+    if (!encode_tensor_map(&maps[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                           const_cast<void*>(ptrs[i]), dims, strides, box,
+                           CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  }
+  SdpaParams p{};
+  p.O = a.O;
+  p.key_lengths = a.key_lengths;
+  p.err = ctl.err;
+  p.limit_ns = ctl.limit_ns;
+  p.B = a.B;
+  p.H = a.H;
+  p.Lq = a.Lq;
+  p.Lk = a.Lk;
+  p.num_q_blocks = (a.Lq + NQT * kBlockM - 1) / (NQT * kBlockM);
+  p.mask_kind = a.mask_kind;
+  p.scale_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
+  p.out_f32 = a.out_dtype == MHA_F32 ? 1 : 0;
+  p.ctx_layout = a.ctx_layout ? 1 : 0;
+  const long long grid = static_cast<long long>(p.num_q_blocks) * a.B * a.H;
+  if (grid <= 0) return cudaSuccess;
+  if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  auto kern = sdpa_fwd_bf16_kernel<D, NQT, NST>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  kern<<<static_cast<unsigned>(grid), C::kThreads, C::kSmemBytes, a.stream>>>(maps[0], maps[1],
+                                                                              maps[2], p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_sdpa_bf16(const SdpaArgs& a, const DeviceCtl& ctl) {
+  // Two query tiles per CTA share every K/V tile (half the K/V traffic per
+  // query row); a single tile when there are too few rows to fill two.
+  const bool two = a.Lq > kBlockM;
+  if (a.d == 64) return two ? launch_impl<64, 2, 3>(a, ctl) : launch_impl<64, 1, 3>(a, ctl);
+  if (a.d == 128) return two ? launch_impl<128, 2, 2>(a, ctl) : launch_impl<128, 1, 2>(a, ctl);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace mha
