@@ -127,6 +127,41 @@ mha_status mha_forward(mha_handle handle, const void *x_q, const void *x_kv,
                        mha_stream stream);
 
 /*
+ * mha_forward_noalloc -- mha_forward for callers that cannot allocate device
+ * memory.  (This entry point has no counterpart in the pages that define
+ * the method; it is a property of this library's interface.)
+ *
+ * mha_forward keeps the projected Q, K, V and the concatenated-heads context
+ * in workspace that mha_create allocates with cudaMalloc.  Callers that must
+ * not call cudaMalloc -- a host program that gives all device memory to its
+ * own pool, a plugin whose execution step may not allocate, a latency-bound
+ * loop that cannot take cudaMalloc's implicit synchronisation -- call this
+ * instead: the same four launches, with those intermediates in a fixed
+ * device array inside the library.  It calls no cudaMalloc, cudaFree or
+ * other allocating routine.
+ *   d_model, dtype : as for mha_create; the other arguments as for
+ *                    mha_forward.
+ * Limit: the intermediates need 2*B*Lq*D + 2*B*Lk*D elements (each tensor
+ * rounded up to 256 bytes); a call needing more than
+ * MHA_NOALLOC_SCRATCH_BYTES returns MHA_ERR_INVALID_ARG and launches
+ * nothing.
+ * The array is held on every GPU that loads the library until the process
+ * exits.  The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture on the device.  All calls on a device share the
+ * array and leave their intermediates in it; calls whose executions overlap
+ * on the GPU (different streams without ordering) race on it.
+ * Returns MHA_OK, MHA_ERR_INVALID_ARG, MHA_ERR_UNSUPPORTED or MHA_ERR_CUDA.
+ */
+#define MHA_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+mha_status mha_forward_noalloc(int d_model, mha_dtype dtype, const void *x_q,
+                               const void *x_kv, const void *Wq,
+                               const void *Wk, const void *Wv, const void *Wo,
+                               int B, int Lq, int Lk, int h, int mask_kind,
+                               const int32_t *key_lengths, void *out,
+                               mha_stream stream);
+
+/*
  * mha_check -- synchronise the current device and report (then clear) its
  * device-side error word.  `handle` may be NULL.  Returns MHA_OK,
  * MHA_ERR_TIMEOUT, MHA_ERR_DEVICE or MHA_ERR_CUDA.

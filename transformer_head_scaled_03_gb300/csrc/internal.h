@@ -64,3 +64,15 @@ bool encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t ran
                        const uint32_t* box, CUtensorMapSwizzle swizzle);
 
 }  // namespace mha
+
+namespace mha {
+
+// The current device's error word and wait limit (false if CUDA fails).
+bool device_ctl(DeviceCtl* ctl);
+
+// The argument checks sdpa_forward applies, for other entry points.
+mha_status validate_sdpa(const void* Q, const void* K, const void* V, const void* O, int B,
+                         int H, int Lq, int Lk, int d, float scale, int mask_kind,
+                         const int32_t* key_lengths, int in_dtype, int out_dtype);
+
+}  // namespace mha

@@ -326,3 +326,17 @@ mha_status mha_destroy(mha_handle h) {
 }
 
 }  // extern "C"
+
+// Accessors for other translation units of the library.
+namespace mha {
+
+bool device_ctl(DeviceCtl* ctl) { return get_device_ctl(ctl); }
+
+mha_status validate_sdpa(const void* Q, const void* K, const void* V, const void* O, int B,
+                         int H, int Lq, int Lk, int d, float scale, int mask_kind,
+                         const int32_t* key_lengths, int in_dtype, int out_dtype) {
+  return check_sdpa(Q, K, V, O, B, H, Lq, Lk, d, scale, mask_kind, key_lengths, in_dtype,
+                    out_dtype);
+}
+
+}  // namespace mha
