@@ -165,6 +165,21 @@ def oracle_cpu_baseline(w, Q, K, V, lens, rows):
     return flops / dt / 1e12, dt, orc.num_threads()
 
 
+def workload_from_args(args):
+    """The chosen workload, optionally with a smaller sequence length or head
+    count (same input recipe) for profiling captures."""
+    import dataclasses
+    from transformer_head_scaled_03_gb300.inputs import WORKLOADS
+    w = WORKLOADS[args.workload]
+    if args.seq is None and args.heads is None:
+        return w
+    L = args.seq if args.seq is not None else w.Lq
+    H = args.heads if args.heads is not None else w.H
+    Lk = L if w.Lq == w.Lk else w.Lk
+    name = f"{w.name.split(' (')[0]} (B{w.B} L{L} H{H} d{w.d} bf16, reduced)"
+    return dataclasses.replace(w, Lq=L, Lk=Lk, H=H, name=name)
+
+
 # ------------------------------------------------------------------ GPU arm
 
 def bench_sdpa(args, w, rank, world, local_rank):
@@ -303,7 +318,7 @@ def run_gpu(args):
         torch.cuda.set_device(local_rank)
         dist.init_process_group(backend="nccl")
     __graft_entry__.build()
-    w = WORKLOADS[args.workload]
+    w = workload_from_args(args)
     r = bench_sdpa(args, w, rank, world, local_rank)
     peaks, peak_src = measured_peaks()
 
@@ -371,7 +386,7 @@ def run_reference(args):
     import oracle
     from transformer_head_scaled_03_gb300.inputs import WORKLOADS, sample_rows, sdpa_inputs
 
-    w = WORKLOADS[args.workload]
+    w = workload_from_args(args)
     Q, K, V, lens, _ = sdpa_inputs(w)
     rows = sample_rows(w.B, w.H, w.Lq, args.ref_rows_per_head, seed=w.seed + 4000, must=())
     for _ in range(args.warmup):
@@ -406,6 +421,10 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--workload", type=int, default=5, choices=[2, 3, 4, 5])
+    ap.add_argument("--seq", type=int, default=None,
+                    help="override the sequence length (profiling captures)")
+    ap.add_argument("--heads", type=int, default=None,
+                    help="override the head count (profiling captures)")
     ap.add_argument("--skip-mha", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--cpu-rows-per-head", type=int, default=32)

@@ -205,48 +205,65 @@ __global__ void __launch_bounds__(Cfg<D, NQT, NST>::kThreads, 1)
     }
   } else if (warp == C::kMmaWarp) {
     // ---------------------------------------------------------- MMA issuer
+    // Issue order per key tile j: PV_0(j), S_0(j+1), PV_1(j), S_1(j+1).
+    // S_t(j+1) overwrites the TMEM columns that P_t(j) occupies; it is
+    // issued after PV_t(j) by the same thread, and tcgen05 MMAs of one CTA
+    // execute in issue order, so PV_t(j) has read P_t(j) before S_t(j+1)
+    // writes.  Each softmax warpgroup thus has two MMAs' time (the other
+    // tile's PV and S) between S_t(j+1) landing and P_t(j+1) being needed.
     if (lane == 0 && n_kv > 0) {
       constexpr uint32_t kIdescQK = idesc_bf16_f32(kBlockM, kBlockN, false, false);
       constexpr uint32_t kIdescPV = idesc_bf16_f32(kBlockM, D, false, true);
-      bool ok = mbar_wait(bar(C::bQ), 0, ctl);
+      auto issue_qk = [&](int t, int st) {
+        const uint32_t qa = base + C::kOffQ + t * C::kTileBytes;
+        const uint32_t kbase = base + C::kOffK + st * C::kTileBytes;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t off = (ks >> 2) * kSub + (ks & 3) * 32;  // 16 elements = 32 bytes
+          umma_ss(tmem + C::tS(t), sdesc_sw128(qa + off, 16, 1024),
+                  sdesc_sw128(kbase + off, 16, 1024), kIdescQK, ks > 0 ? 1u : 0u);
+        }
+      };
+      auto issue_pv = [&](int t, int st, bool accumulate) {
+        const uint32_t vbase = base + C::kOffV + st * C::kTileBytes;
+#pragma unroll
+        for (int ks = 0; ks < kBlockN / 16; ++ks) {
+          // 16 keys of V = 16 rows of 128 bytes; P: 16 bf16 = 8 TMEM columns
+          umma_ts(tmem + C::tO(t), tmem + C::tS(t) + ks * 8,
+                  sdesc_sw128(vbase + ks * 16 * 128, kSub, 1024), kIdescPV,
+                  (accumulate || ks > 0) ? 1u : 0u);
+        }
+      };
+      bool ok = mbar_wait(bar(C::bQ), 0, ctl) && mbar_wait(bar(C::bKF(0)), 0, ctl);
+      if (ok) {
+        tc_fence_after();
+        for (int t = 0; t < NQT; ++t) {
+          issue_qk(t, 0);
+          umma_commit(bar(C::bS(t)));
+        }
+        umma_commit(bar(C::bKE(0)));
+      }
       for (int j = 0; ok && j < n_kv; ++j) {
         const int st = j % NST;
         const uint32_t ph = (j / NST) & 1;
-        if (!(ok = mbar_wait(bar(C::bKF(st)), ph, ctl))) break;
-        tc_fence_after();
-        for (int t = 0; t < NQT && ok; ++t) {
-          // S_t aliases P_t of the previous tile: wait until that P.V is done
-          if (j > 0) {
-            if (!(ok = mbar_wait(bar(C::bO(t)), (j - 1) & 1, ctl))) break;
-            tc_fence_after();
-          }
-          const uint32_t qa = base + C::kOffQ + t * C::kTileBytes;
-          const uint32_t kbase = base + C::kOffK + st * C::kTileBytes;
-#pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks) {
-            const uint32_t off = (ks >> 2) * kSub + (ks & 3) * 32;  // 16 elements = 32 bytes
-            umma_ss(tmem + C::tS(t), sdesc_sw128(qa + off, 16, 1024),
-                    sdesc_sw128(kbase + off, 16, 1024), kIdescQK, ks > 0 ? 1u : 0u);
-          }
-          umma_commit(bar(C::bS(t)));
-        }
-        if (!ok) break;
-        umma_commit(bar(C::bKE(st)));
+        const bool more = j + 1 < n_kv;
+        const int st1 = (j + 1) % NST;
+        const uint32_t ph1 = ((j + 1) / NST) & 1;
         if (!(ok = mbar_wait(bar(C::bVF(st)), ph, ctl))) break;
-        const uint32_t vbase = base + C::kOffV + st * C::kTileBytes;
         for (int t = 0; t < NQT && ok; ++t) {
           if (!(ok = mbar_wait(bar(C::bP(t)), j & 1, ctl))) break;
           tc_fence_after();
-#pragma unroll
-          for (int ks = 0; ks < kBlockN / 16; ++ks) {
-            // 16 keys of V = 16 rows of 128 bytes; P: 16 bf16 = 8 TMEM columns
-            umma_ts(tmem + C::tO(t), tmem + C::tS(t) + ks * 8,
-                    sdesc_sw128(vbase + ks * 16 * 128, kSub, 1024), kIdescPV,
-                    (j > 0 || ks > 0) ? 1u : 0u);
+          issue_pv(t, st, j > 0);
+          if (!more) {
+            umma_commit(bar(C::bO(t)));
+            continue;
           }
-          umma_commit(bar(C::bO(t)));
+          if (t == 0 && !(ok = mbar_wait(bar(C::bKF(st1)), ph1, ctl))) break;
+          issue_qk(t, st1);
+          umma_commit(bar(C::bS(t)));
         }
         if (!ok) break;
+        if (more) umma_commit(bar(C::bKE(st1)));
         umma_commit(bar(C::bVE(st)));
       }
       // every issued MMA completes before tensor memory is released
@@ -263,8 +280,14 @@ __global__ void __launch_bounds__(Cfg<D, NQT, NST>::kThreads, 1)
     const uint32_t tS = tmem + lane_bits + C::tS(t);
     const uint32_t tO = tmem + lane_bits + C::tO(t);
     const float sl2 = p.scale_log2;
-    float m = -INFINITY;  // running max of the raw (unscaled, masked) scores
-    float l = 0.f;        // running sum of 2^((s - m) * sl2)
+    // m_ref: the reference maximum (raw score units) that p = 2^((s - m_ref)
+    // * sl2) is taken against.  It is raised only when a tile's maximum
+    // exceeds it by more than kRescaleLog2 (in log2 units); below that the
+    // stale reference is kept and p may reach 2^kRescaleLog2.  O and l share
+    // the reference, so O / l is unchanged.
+    constexpr float kRescaleLog2 = 8.f;
+    float m_ref = -INFINITY;
+    float l = 0.f;
     bool ok = true;
     for (int j = 0; j < n_kv; ++j) {
       if (!(ok = mbar_wait_warp(bar(C::bS(t)), j & 1, ctl))) break;
@@ -288,29 +311,47 @@ __global__ void __launch_bounds__(Cfg<D, NQT, NST>::kThreads, 1)
           if (key >= key_end || (causal && key > q_row)) x[c] = -INFINITY;
         }
       }
-      float mt = x[0];
+      // tile maximum: eight independent 3-input max chains, then combine
+      float m8[8];
 #pragma unroll
-      for (int c = 1; c < 128; ++c) mt = fmaxf(mt, x[c]);
-      const float m_new = fmaxf(m, mt);
-      const float alpha = (m_new == -INFINITY) ? 1.f : ex2_approx((m - m_new) * sl2);
-      l *= alpha;
-      m = m_new;
-      const float mb = (m == -INFINITY) ? 0.f : m * sl2;
-      float rs = 0.f;
+      for (int i = 0; i < 8; ++i) m8[i] = fmax3(x[i], x[8 + i], x[16 + i]);
+#pragma unroll
+      for (int c = 24; c < 120; c += 16)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) m8[i] = fmax3(m8[i], x[c + i], x[c + 8 + i]);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) m8[i] = fmaxf(m8[i], x[120 + i]);
+      const float mt = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]),
+                             fmaxf(m8[6], m8[7]));
+      float alpha = 1.f;
+      if (mt > m_ref && (m_ref == -INFINITY || (mt - m_ref) * sl2 > kRescaleLog2)) {
+        alpha = ex2_approx((m_ref - mt) * sl2);  // 0 when m_ref = -inf
+        m_ref = mt;
+        l *= alpha;
+      }
+      const float mb = (m_ref == -INFINITY) ? 0.f : m_ref * sl2;
+      // p = 2^(s*sl2 - mb), two at a time; four independent partial sums
+      const float2 scale2 = make_float2(sl2, sl2);
+      const float2 shift2 = make_float2(-mb, -mb);
+      float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                       make_float2(0.f, 0.f)};
       uint32_t pk[64];
 #pragma unroll
       for (int c = 0; c < 64; ++c) {
-        const float p0 = ex2_approx(fmaf(x[2 * c], sl2, -mb));
-        const float p1 = ex2_approx(fmaf(x[2 * c + 1], sl2, -mb));
-        rs += p0 + p1;
-        pk[c] = pack_bf16x2(p0, p1);
+        const float2 e = ffma2(make_float2(x[2 * c], x[2 * c + 1]), scale2, shift2);
+        const float2 pp = make_float2(ex2_approx(e.x), ex2_approx(e.y));
+        acc[c & 3] = fadd2(acc[c & 3], pp);
+        pk[c] = pack_bf16x2(pp.x, pp.y);
       }
-      l += rs;
+      const float2 a01 = fadd2(acc[0], acc[1]), a23 = fadd2(acc[2], acc[3]);
+      const float2 a = fadd2(a01, a23);
+      l += a.x + a.y;
       tmem_st32(tS + 0, *reinterpret_cast<const uint32_t(*)[32]>(&pk[0]));
       tmem_st32(tS + 32, *reinterpret_cast<const uint32_t(*)[32]>(&pk[32]));
-      // Rescale the partial output when the running max grew.  P.V of the
-      // previous tile is complete: its commit preceded this tile's S commit.
-      // Done after P is stored, when the score registers are free again.
+      // Rescale the partial output when the reference max moved.  P.V of the
+      // previous tile is complete: it was issued before this tile's S, whose
+      // commit covers it.  Done after P is stored, when the score registers
+      // are free again.
       if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
         for (int cb = 0; cb < D / 32; ++cb) {
@@ -329,7 +370,7 @@ __global__ void __launch_bounds__(Cfg<D, NQT, NST>::kThreads, 1)
     // ------------------------------------------------------------ epilogue
     bool have = ok && n_kv > 0;
     if (have) {
-      have = mbar_wait_warp(bar(C::bO(t)), (n_kv - 1) & 1, ctl);
+      have = mbar_wait_warp(bar(C::bO(t)), 0, ctl);
       tc_fence_after();
     }
     const float inv_l = (have && l > 0.f) ? 1.f / l : 0.f;
