@@ -214,24 +214,32 @@ __global__ void __launch_bounds__(Cfg<D, NQT, NST>::kThreads, 1)
     if (lane == 0 && n_kv > 0) {
       constexpr uint32_t kIdescQK = idesc_bf16_f32(kBlockM, kBlockN, false, false);
       constexpr uint32_t kIdescPV = idesc_bf16_f32(kBlockM, D, false, true);
+      // Descriptors are built once; per MMA only a compile-time offset (in
+      // 16-byte units, the descriptor's address granule) is added, which
+      // keeps the single issuing thread off long integer chains.
+      const uint64_t q_desc = sdesc_sw128(base + C::kOffQ, 16, 1024);
+      const uint64_t k_desc = sdesc_sw128(base + C::kOffK, 16, 1024);
+      const uint64_t v_desc = sdesc_sw128(base + C::kOffV, kSub, 1024);
       auto issue_qk = [&](int t, int st) {
-        const uint32_t qa = base + C::kOffQ + t * C::kTileBytes;
-        const uint32_t kbase = base + C::kOffK + st * C::kTileBytes;
+        const uint64_t qd = q_desc + static_cast<uint64_t>((t * C::kTileBytes) >> 4);
+        const uint64_t kd = k_desc + static_cast<uint64_t>((st * C::kTileBytes) >> 4);
+        const uint32_t d_tmem = tmem + C::tS(t);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t off = (ks >> 2) * kSub + (ks & 3) * 32;  // 16 elements = 32 bytes
-          umma_ss(tmem + C::tS(t), sdesc_sw128(qa + off, 16, 1024),
-                  sdesc_sw128(kbase + off, 16, 1024), kIdescQK, ks > 0 ? 1u : 0u);
+          // 16 elements = 32 bytes inside a 128-byte row; 64-column blocks kSub apart
+          const uint64_t off = static_cast<uint64_t>(((ks >> 2) * kSub + (ks & 3) * 32) >> 4);
+          umma_ss(d_tmem, qd + off, kd + off, kIdescQK, ks > 0 ? 1u : 0u);
         }
       };
-      auto issue_pv = [&](int t, int st, bool accumulate) {
-        const uint32_t vbase = base + C::kOffV + st * C::kTileBytes;
+      auto issue_pv = [&](int t, int st, uint32_t accumulate) {
+        const uint64_t vd = v_desc + static_cast<uint64_t>((st * C::kTileBytes) >> 4);
+        const uint32_t d_tmem = tmem + C::tO(t);
+        const uint32_t a_tmem = tmem + C::tS(t);
 #pragma unroll
         for (int ks = 0; ks < kBlockN / 16; ++ks) {
           // 16 keys of V = 16 rows of 128 bytes; P: 16 bf16 = 8 TMEM columns
-          umma_ts(tmem + C::tO(t), tmem + C::tS(t) + ks * 8,
-                  sdesc_sw128(vbase + ks * 16 * 128, kSub, 1024), kIdescPV,
-                  (accumulate || ks > 0) ? 1u : 0u);
+          umma_ts(d_tmem, a_tmem + ks * 8, vd + static_cast<uint64_t>((ks * 16 * 128) >> 4),
+                  kIdescPV, ks > 0 ? 1u : accumulate);
         }
       };
       bool ok = mbar_wait(bar(C::bQ), 0, ctl) && mbar_wait(bar(C::bKF(0)), 0, ctl);
@@ -253,7 +261,7 @@ __global__ void __launch_bounds__(Cfg<D, NQT, NST>::kThreads, 1)
         for (int t = 0; t < NQT && ok; ++t) {
           if (!(ok = mbar_wait(bar(C::bP(t)), j & 1, ctl))) break;
           tc_fence_after();
-          issue_pv(t, st, j > 0);
+          issue_pv(t, st, j > 0 ? 1u : 0u);
           if (!more) {
             umma_commit(bar(C::bO(t)));
             continue;
@@ -292,57 +300,67 @@ __global__ void __launch_bounds__(Cfg<D, NQT, NST>::kThreads, 1)
     for (int j = 0; j < n_kv; ++j) {
       if (!(ok = mbar_wait_warp(bar(C::bS(t)), j & 1, ctl))) break;
       tc_fence_after();
-      uint32_t s[128];
-      tmem_ld32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
-      tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
-      tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(&s[64]));
-      tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(&s[96]));
-      tmem_ld_wait(s);
-      float x[128];
-#pragma unroll
-      for (int c = 0; c < 128; ++c) x[c] = __uint_as_float(s[c]);
       const int k0 = j * kBlockN;
       const bool edge = (k0 + kBlockN > key_end) ||
                         (causal && k0 + kBlockN - 1 > q0 + t * kBlockM);
-      if (edge) {
+      // visible keys of this row in this tile: columns c <= last
+      int last = key_end - 1 - k0;
+      if (causal) last = min(last, q_row - k0);
+      // S row -> registers (masked)
+      auto load_scores = [&](float (&x)[128]) {
+        uint32_t s[128];
+        tmem_ld32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
+        tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
+        tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(&s[64]));
+        tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(&s[96]));
+        tmem_ld_wait(s);
 #pragma unroll
-        for (int c = 0; c < 128; ++c) {
-          const int key = k0 + c;
-          if (key >= key_end || (causal && key > q_row)) x[c] = -INFINITY;
+        for (int c = 0; c < 128; ++c) x[c] = __uint_as_float(s[c]);
+        if (edge) {
+#pragma unroll
+          for (int c = 0; c < 128; ++c) x[c] = c <= last ? x[c] : -INFINITY;
         }
-      }
+      };
       // tile maximum: eight independent 3-input max chains, then combine
-      float m8[8];
+      auto tile_max = [&](const float (&x)[128]) -> float {
+        float m8[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) m8[i] = fmax3(x[i], x[8 + i], x[16 + i]);
+        for (int i = 0; i < 8; ++i) m8[i] = fmax3(x[i], x[8 + i], x[16 + i]);
 #pragma unroll
-      for (int c = 24; c < 120; c += 16)
+        for (int c = 24; c < 120; c += 16)
 #pragma unroll
-        for (int i = 0; i < 8; ++i) m8[i] = fmax3(m8[i], x[c + i], x[c + 8 + i]);
+          for (int i = 0; i < 8; ++i) m8[i] = fmax3(m8[i], x[c + i], x[c + 8 + i]);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) m8[i] = fmaxf(m8[i], x[120 + i]);
-      const float mt = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]),
-                             fmaxf(m8[6], m8[7]));
+        for (int i = 0; i < 8; ++i) m8[i] = fmaxf(m8[i], x[120 + i]);
+        return fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]),
+                     fmaxf(m8[6], m8[7]));
+      };
+      // p = 2^(s*sl2 - mb), two at a time with four independent partial sums
+      auto exps = [&](const float (&x)[128], float mb, float2 (&acc)[4], uint32_t (&pk)[64]) {
+        const float2 scale2 = make_float2(sl2, sl2);
+        const float2 shift2 = make_float2(-mb, -mb);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[i] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          const float2 e = ffma2(make_float2(x[2 * c], x[2 * c + 1]), scale2, shift2);
+          const float2 pp = make_float2(ex2_approx(e.x), ex2_approx(e.y));
+          acc[c & 3] = fadd2(acc[c & 3], pp);
+          pk[c] = pack_bf16x2(pp.x, pp.y);
+        }
+      };
+      float x[128];
+      float2 acc[4];
+      uint32_t pk[64];
       float alpha = 1.f;
+      load_scores(x);
+      const float mt = tile_max(x);
       if (mt > m_ref && (m_ref == -INFINITY || (mt - m_ref) * sl2 > kRescaleLog2)) {
         alpha = ex2_approx((m_ref - mt) * sl2);  // 0 when m_ref = -inf
         m_ref = mt;
         l *= alpha;
       }
-      const float mb = (m_ref == -INFINITY) ? 0.f : m_ref * sl2;
-      // p = 2^(s*sl2 - mb), two at a time; four independent partial sums
-      const float2 scale2 = make_float2(sl2, sl2);
-      const float2 shift2 = make_float2(-mb, -mb);
-      float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                       make_float2(0.f, 0.f)};
-      uint32_t pk[64];
-#pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        const float2 e = ffma2(make_float2(x[2 * c], x[2 * c + 1]), scale2, shift2);
-        const float2 pp = make_float2(ex2_approx(e.x), ex2_approx(e.y));
-        acc[c & 3] = fadd2(acc[c & 3], pp);
-        pk[c] = pack_bf16x2(pp.x, pp.y);
-      }
+      exps(x, m_ref == -INFINITY ? 0.f : m_ref * sl2, acc, pk);
       const float2 a01 = fadd2(acc[0], acc[1]), a23 = fadd2(acc[2], acc[3]);
       const float2 a = fadd2(a01, a23);
       l += a.x + a.y;
@@ -461,6 +479,7 @@ cudaError_t launch_impl(const SdpaArgs& a, const DeviceCtl& ctl) {
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
+
   kern<<<static_cast<unsigned>(grid), C::kThreads, C::kSmemBytes, a.stream>>>(maps[0], maps[1],
                                                                               maps[2], p);
   return cudaGetLastError();
