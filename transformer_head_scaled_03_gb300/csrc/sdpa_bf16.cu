@@ -148,13 +148,15 @@ __global__ void __launch_bounds__(Cfg<D, NQT, NST>::kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
 
-  // ---- which (b, h, query block) this CTA computes; causal blocks are
-  // visited longest-first so the short ones fill the tail of the grid.
-  const int BH = p.B * p.H;
+  // ---- which (b, h, query block) this CTA computes.  Head-major order:
+  // consecutive CTAs take the query blocks of one head, so the CTAs resident
+  // at any moment share one or two heads' K/V in L2 instead of streaming
+  // every head's K/V from HBM.  Causal blocks of a head go longest-first so
+  // the short ones fill the tail of the grid.
   const bool causal = (p.mask_kind & MHA_MASK_CAUSAL) != 0;
   const bool padded = (p.mask_kind & MHA_MASK_KEY_PADDING) != 0;
-  const int blk = static_cast<int>(blockIdx.x) / BH;
-  const int bh = static_cast<int>(blockIdx.x) - blk * BH;
+  const int bh = static_cast<int>(blockIdx.x) / p.num_q_blocks;
+  const int blk = static_cast<int>(blockIdx.x) - bh * p.num_q_blocks;
   const int qb = causal ? (p.num_q_blocks - 1 - blk) : blk;
   const int b = bh / p.H;
   const int h = bh - b * p.H;
