@@ -304,27 +304,49 @@ def bench_mha_layer(w_shape, dtype_name, steps, warmup, local_rank, seed_w=None)
     try:
         def step():
             mha.mha_forward(handle, x, x, *Ws, h=h, out=out)
+
+        def timed(fn, n):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(n):
+                fn()
+            e1.record()
+            torch.cuda.synchronize()
+            return e0.elapsed_time(e1) / n
+
         for _ in range(warmup):
             step()
         torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for _ in range(steps):
+        eager_ms = timed(step, steps)
+        # the same call captured once in a CUDA graph and replayed: the
+        # library's device time without the per-call host overhead
+        graph = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
             step()
-        e1.record()
+        torch.cuda.current_stream().wait_stream(side)
+        with torch.cuda.graph(graph):
+            step()
+        for _ in range(warmup):
+            graph.replay()
         torch.cuda.synchronize()
+        graph_ms = timed(graph.replay, steps)
         st = mha.mha_check(handle)
         if st != mha.MHA_OK:
             raise RuntimeError(mha.status_string(st))
-        ms = e0.elapsed_time(e1) / steps
     finally:
         handle.close()
     d = D // h
     proj_flops = 4 * 2.0 * B * L * D * D
     attn_flops = 4.0 * B * h * L * L * d
     return {"shape": {"B": B, "L": L, "D": D, "h": h, "dtype": dtype_name, "mask": "none"},
-            "tokens_per_s": round(B * L / (ms / 1e3), 1), "ms_per_layer": round(ms, 4),
-            "tflops": round((proj_flops + attn_flops) / (ms / 1e3) / 1e12, 2),
+            "tokens_per_s": round(B * L / (graph_ms / 1e3), 1),
+            "ms_per_layer": round(graph_ms, 4),
+            "tflops": round((proj_flops + attn_flops) / (graph_ms / 1e3) / 1e12, 2),
+            "timing": "CUDA graph replay of one mha_forward call",
+            "eager_tokens_per_s": round(B * L / (eager_ms / 1e3), 1),
+            "eager_ms_per_layer": round(eager_ms, 4),
             "gpu_launches_per_layer": 3}
 
 
@@ -345,8 +367,8 @@ def run_gpu(args):
 
     mha_layer = None
     if not args.skip_mha:
-        mha_layer = [bench_mha_layer((w.B, w.Lq, w.H * w.d, w.H), "bf16", 3, 2, local_rank),
-                     bench_mha_layer((1, 128, 512, 8), "f32", 50, 5, local_rank,
+        mha_layer = [bench_mha_layer((w.B, w.Lq, w.H * w.d, w.H), "bf16", 3, 3, local_rank),
+                     bench_mha_layer((1, 128, 512, 8), "f32", 200, 5, local_rank,
                                      seed_w=WORKLOADS[1].seed)]
 
     cpu = None

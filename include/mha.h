@@ -168,6 +168,18 @@ mha_status mha_forward_noalloc(int d_model, mha_dtype dtype, const void *x_q,
  */
 mha_status mha_check(mha_handle handle);
 
+/*
+ * mha_selftest_wait_timeout -- exercise the failure path of the kernels'
+ * bounded waits: launches one warp that waits on a shared-memory mbarrier
+ * nothing arrives on, using the same wait routine as the attention and GEMM
+ * pipelines, with a limit of `limit_ms` (1..10000).  The wait gives up, the
+ * kernel sets MHA_ERR_TIMEOUT in the device error word and returns; a later
+ * mha_check() reports (and clears) it and the context stays usable.  (A
+ * property of this library's interface; the pages have no counterpart.)
+ * Returns MHA_OK (launched), MHA_ERR_INVALID_ARG or MHA_ERR_CUDA.
+ */
+mha_status mha_selftest_wait_timeout(int limit_ms, mha_stream stream);
+
 /* mha_destroy -- free the handle and its workspace (synchronises the
  * device first).  NULL is accepted. */
 mha_status mha_destroy(mha_handle handle);

@@ -59,6 +59,8 @@ def _declare(lib):
     lib.mha_status_string.restype = ctypes.c_char_p
     lib.mha_set_wait_limit_ms.argtypes = [i32]
     lib.mha_set_wait_limit_ms.restype = i32
+    lib.mha_selftest_wait_timeout.argtypes = [i32, vp]
+    lib.mha_selftest_wait_timeout.restype = i32
     return lib
 
 
@@ -192,6 +194,13 @@ def mha_check(handle: MhaHandle | None = None) -> int:
 
 def mha_destroy(handle: MhaHandle):
     handle.close()
+
+
+def selftest_wait_timeout(limit_ms: int = 100, stream=None):
+    """Launch the bounded-wait self-test (see include/mha.h); mha_check() then
+    reports MHA_ERR_TIMEOUT."""
+    _check(lib().mha_selftest_wait_timeout(int(limit_ms), _stream(stream)),
+           "mha_selftest_wait_timeout")
 
 
 def set_wait_limit_ms(ms: int) -> int:

@@ -87,6 +87,27 @@ bool encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t ran
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+namespace {
+
+// Self-test of the bounded pipeline wait: one warp waits on an mbarrier that
+// nothing ever arrives on, with the same helper the attention and GEMM
+// kernels use.  The wait must give up after the limit, raise the abort flag
+// and set the timeout bit in the device error word, and the kernel returns.
+__global__ void wait_selftest_kernel(unsigned* err, uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ volatile int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const WaitCtl ctl{&abort_flag, err, limit_ns};
+  mbar_wait_warp(smem_u32(&bar), 0, ctl);
+}
+
+}  // namespace
+
 }  // namespace mha
 
 using namespace mha;
@@ -295,6 +316,15 @@ mha_status mha_forward(mha_handle h, const void* x_q, const void* x_kv, const vo
   go.dtype = h->dtype;
   go.stream = s;
   return from_cuda(gemm(go, ctl));
+}
+
+mha_status mha_selftest_wait_timeout(int limit_ms, mha_stream stream) {
+  if (limit_ms < 1 || limit_ms > 10000) return MHA_ERR_INVALID_ARG;
+  DeviceCtl ctl;
+  if (!get_device_ctl(&ctl)) return MHA_ERR_CUDA;
+  wait_selftest_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      ctl.err, static_cast<uint64_t>(limit_ms) * 1000000ull);
+  return from_cuda(cudaGetLastError());
 }
 
 mha_status mha_check(mha_handle) {
