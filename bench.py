@@ -373,12 +373,13 @@ def run_gpu(args):
 
     cpu = None
     if rank == 0 and not args.skip_cpu:
-        rows = sample_rows(w.B, w.H, w.Lq, args.cpu_rows_per_head, seed=w.seed + 3000,
-                           must=())
+        # about 10 s of fp64 oracle work on a 16-core host
+        per_head = args.cpu_rows_per_head or {2: 48, 3: 256, 4: 96, 5: 512}[args.workload]
+        rows = sample_rows(w.B, w.H, w.Lq, min(per_head, w.Lq), seed=w.seed + 3000, must=())
         tf, dt, cores = oracle_cpu_baseline(w, r["Q"], r["K"], r["V"], r["lens"], rows)
         cpu = {"value": round(tf, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                "seconds": round(dt, 2),
-               "sample": f"{rows.size} query rows ({args.cpu_rows_per_head} per head, all "
+               "sample": f"{rows.size} query rows ({min(per_head, w.Lq)} per head, all "
                          f"{w.B * w.H} heads, seeded) of the same workload, fp64"}
 
     if rank != 0:
@@ -475,7 +476,8 @@ def main(argv=None):
                     help="override the head count (profiling captures)")
     ap.add_argument("--skip-mha", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
-    ap.add_argument("--cpu-rows-per-head", type=int, default=32)
+    ap.add_argument("--cpu-rows-per-head", type=int, default=None,
+                    help="oracle CPU-baseline sample (default: about 10 s of work)")
     ap.add_argument("--ref-rows-per-head", type=int, default=4)
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per launch of the fused kernel from an ncu capture")

@@ -78,7 +78,8 @@ def test_mha_base_shape_fp32_workload():
     finally:
         handle.close()
     ref = oracle.mha(x, x, Wq, Wk, Wv, Wo, h=w.H)
-    assert_parity(got, ref, torch.float32, "base-shape fp32 layer")
+    max_abs, rms = assert_parity(got, ref, torch.float32, "base-shape fp32 layer")
+    print(f"\n{w.name}: all {got.size} outputs, max|err| {max_abs:.3e}, rms rel {rms:.3e}")
 
 
 def test_mha_rejects_sizes_above_handle_maxima():
