@@ -50,12 +50,13 @@ def _declare(lib):
     ip = ctypes.POINTER(ctypes.c_int32)
     lp = ctypes.POINTER(ctypes.c_int64)
     c_int, c_double = ctypes.c_int, ctypes.c_double
+    c_i64 = ctypes.c_int64
     lib.oracle_sdpa.argtypes = [dp, dp, dp, dp, dp, c_int, c_int, c_int, c_int,
-                                c_int, c_double, c_int, ip, c_int]
+                                c_int, c_double, c_int, ip, dp, c_i64, c_i64, c_int]
     lib.oracle_sdpa.restype = c_int
     lib.oracle_sdpa_rows.argtypes = [dp, dp, dp, dp, lp, c_int, c_int, c_int,
                                      c_int, c_int, c_int, c_double, c_int, ip,
-                                     c_int]
+                                     dp, c_i64, c_i64, c_int]
     lib.oracle_sdpa_rows.restype = c_int
     lib.oracle_mha.argtypes = [dp, dp, dp, dp, dp, dp, dp, c_int, c_int, c_int,
                                c_int, c_int, c_int, ip, c_int]
@@ -91,6 +92,22 @@ def _ptr(a: np.ndarray, ctype=ctypes.c_double):
     return a.ctypes.data_as(ctypes.POINTER(ctype))
 
 
+def _add_mask(add_mask, B: int, H: int, Lq: int, Lk: int):
+    """Additive float mask broadcastable to [B, H, Lq, Lk] -> (array, its
+    pointer, batch stride, head stride) in elements; strides 0 broadcast."""
+    if add_mask is None:
+        return None, None, 0, 0
+    a = np.asarray(add_mask, dtype=np.float64)
+    while a.ndim < 4:
+        a = a[None]
+    if a.shape[2:] != (Lq, Lk) or a.shape[0] not in (1, B) or a.shape[1] not in (1, H):
+        raise ValueError("additive mask must broadcast to [B, H, Lq, Lk]")
+    a = np.ascontiguousarray(a)
+    sb = a.shape[1] * Lq * Lk if a.shape[0] == B and B > 1 else 0
+    sh = Lq * Lk if a.shape[1] == H and H > 1 else 0
+    return a, _ptr(a), sb, sh
+
+
 def _lengths(mask_kind: int, key_lengths, B: int):
     if mask_kind & MASK_KEY_PADDING:
         kl = np.ascontiguousarray(np.asarray(key_lengths, dtype=np.int32))
@@ -110,8 +127,12 @@ class Oracle:
         return int(self.lib.oracle_num_threads())
 
     def sdpa(self, Q, K, V, scale: float = 0.0, mask_kind: int = MASK_NONE,
-             key_lengths=None, return_weights: bool = False, nthreads: int = 0):
-        """Q [B,H,Lq,d], K/V [B,H,Lk,d] -> O [B,H,Lq,d] (and weights [B,H,Lq,Lk])."""
+             key_lengths=None, return_weights: bool = False, nthreads: int = 0,
+             add_mask=None):
+        """Q [B,H,Lq,d], K/V [B,H,Lk,d] -> O [B,H,Lq,d] (and weights [B,H,Lq,Lk]).
+
+        ``add_mask``: optional float mask broadcastable to [B,H,Lq,Lk], added
+        to the scaled scores."""
         Q, K, V = _d(Q), _d(K), _d(V)
         B, H, Lq, d = Q.shape
         Lk = K.shape[2]
@@ -120,16 +141,17 @@ class Oracle:
         O = np.empty((B, H, Lq, d))
         W = np.empty((B, H, Lq, Lk)) if return_weights else None
         kl, klp = _lengths(mask_kind, key_lengths, B)
+        am, amp, sb, sh = _add_mask(add_mask, B, H, Lq, Lk)
         bad = self.lib.oracle_sdpa(_ptr(Q), _ptr(K), _ptr(V), _ptr(O),
                                    _ptr(W) if W is not None else None, B, H, Lq,
-                                   Lk, d, float(scale), int(mask_kind), klp,
-                                   int(nthreads))
+                                   Lk, d, float(scale), int(mask_kind), klp, amp,
+                                   sb, sh, int(nthreads))
         self.last_bad_rows = int(bad)
         return (O, W) if return_weights else O
 
     def sdpa_rows(self, Q, K, V, rows, scale: float = 0.0,
                   mask_kind: int = MASK_NONE, key_lengths=None,
-                  nthreads: int = 0):
+                  nthreads: int = 0, add_mask=None):
         """Rows ``rows`` (flat (b*H+h)*Lq+i) of the attention output -> [n, d]."""
         Q, K, V = _d(Q), _d(K), _d(V)
         B, H, Lq, d = Q.shape
@@ -137,10 +159,12 @@ class Oracle:
         r = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
         out = np.empty((r.size, d))
         kl, klp = _lengths(mask_kind, key_lengths, B)
+        am, amp, sb, sh = _add_mask(add_mask, B, H, Lq, Lk)
         bad = self.lib.oracle_sdpa_rows(_ptr(Q), _ptr(K), _ptr(V), _ptr(out),
                                         _ptr(r, ctypes.c_int64), int(r.size), B,
                                         H, Lq, Lk, d, float(scale),
-                                        int(mask_kind), klp, int(nthreads))
+                                        int(mask_kind), klp, amp, sb, sh,
+                                        int(nthreads))
         self.last_bad_rows = int(bad)
         return out
 

@@ -20,6 +20,10 @@
  *   triangle, as in the printed 4x4 mask of that section).
  *   Key padding: key j is blocked for every query of batch item b when
  *   j >= key_lengths[b] (one row of the mask per batch item, same section).
+ *   Additive float mask: an optional [Lq, Lk] array A (per batch item and
+ *   head through strides, 0 to broadcast) added to the scaled scores like
+ *   the causal mask's 0/-inf entries are -- the optional mask of the
+ *   reference SDPA the same page describes ("Attention, by hand").
  *
  *   MultiHead(x_q, x_kv) = Concat(head_1, ..., head_h) W^O,
  *   head_i = Attention(x_q W^Q_i, x_kv W^K_i, x_kv W^V_i)
@@ -75,14 +79,17 @@ static double mask_entry(int i, int j, int mask_kind, int len_b)
 static int attend_row(const double *q, const double *K, ptrdiff_t ldk,
                       const double *V, ptrdiff_t ldv, int Lk, int d,
                       double scale, int i, int mask_kind, int len_b,
-                      double *w, double *o)
+                      const double *add_row, double *w, double *o)
 {
-    /* scores s_j = scale * <q, k_j> + M_ij */
+    /* scores s_j = scale * <q, k_j> + M_ij (+ A_ij, an additive float mask
+     * row given by the caller, when add_row is not NULL) */
     for (int j = 0; j < Lk; ++j) {
         double dot = 0.0;
         for (int c = 0; c < d; ++c)
             dot += q[c] * K[(ptrdiff_t)j * ldk + c];
         w[j] = scale * dot + mask_entry(i, j, mask_kind, len_b);
+        if (add_row)
+            w[j] += add_row[j];
     }
     /* row maximum */
     double m = -INFINITY;
@@ -131,7 +138,8 @@ static int len_of(const int32_t *key_lengths, int mask_kind, int b, int Lk)
  */
 int oracle_sdpa(const double *Q, const double *K, const double *V, double *O,
                 double *W, int B, int H, int Lq, int Lk, int d, double scale,
-                int mask_kind, const int32_t *key_lengths, int nthreads)
+                int mask_kind, const int32_t *key_lengths, const double *add_mask,
+                int64_t add_stride_b, int64_t add_stride_h, int nthreads)
 {
     const double sc = resolve_scale(scale, d);
     int bad = 0;
@@ -148,9 +156,13 @@ int oracle_sdpa(const double *Q, const double *K, const double *V, double *O,
         const double *Kh = K + (size_t)bh * Lk * d;
         const double *Vh = V + (size_t)bh * Lk * d;
         double *wrow = (double *)malloc(sizeof(double) * (size_t)(Lk > 0 ? Lk : 1));
+        const int hh = (int)(bh % H);
         for (int i = 0; i < Lq; ++i) {
+            const double *arow = add_mask ? add_mask + (int64_t)b * add_stride_b +
+                                                (int64_t)hh * add_stride_h + (int64_t)i * Lk
+                                          : NULL;
             bad += attend_row(Qh + (size_t)i * d, Kh, d, Vh, d, Lk, d, sc, i,
-                              mask_kind, len_b, wrow, O + ((size_t)bh * Lq + i) * d);
+                              mask_kind, len_b, arow, wrow, O + ((size_t)bh * Lq + i) * d);
             if (W)
                 memcpy(W + ((size_t)bh * Lq + i) * Lk, wrow, sizeof(double) * (size_t)Lk);
         }
@@ -167,7 +179,8 @@ int oracle_sdpa(const double *Q, const double *K, const double *V, double *O,
 int oracle_sdpa_rows(const double *Q, const double *K, const double *V,
                      double *O_rows, const int64_t *rows, int nrows, int B,
                      int H, int Lq, int Lk, int d, double scale, int mask_kind,
-                     const int32_t *key_lengths, int nthreads)
+                     const int32_t *key_lengths, const double *add_mask,
+                     int64_t add_stride_b, int64_t add_stride_h, int nthreads)
 {
     const double sc = resolve_scale(scale, d);
     int bad = 0;
@@ -183,10 +196,14 @@ int oracle_sdpa_rows(const double *Q, const double *K, const double *V,
         const int i = (int)(rows[r] % Lq);
         const int b = (int)(bh / H);
         const int len_b = len_of(key_lengths, mask_kind, b, Lk);
+        const int hh = (int)(bh % H);
+        const double *arow = add_mask ? add_mask + (int64_t)b * add_stride_b +
+                                            (int64_t)hh * add_stride_h + (int64_t)i * Lk
+                                      : NULL;
         double *wrow = (double *)malloc(sizeof(double) * (size_t)(Lk > 0 ? Lk : 1));
         bad += attend_row(Q + (size_t)rows[r] * d, K + (size_t)bh * Lk * d, d,
                           V + (size_t)bh * Lk * d, d, Lk, d, sc, i, mask_kind,
-                          len_b, wrow, O_rows + (size_t)r * d);
+                          len_b, arow, wrow, O_rows + (size_t)r * d);
         free(wrow);
     }
     return bad;
@@ -250,7 +267,7 @@ int oracle_mha(const double *x_q, const double *x_kv, const double *Wq,
             const double *Kh = Kp + (size_t)b * Lk * D + (size_t)hh * d;
             const double *Vh = Vp + (size_t)b * Lk * D + (size_t)hh * d;
             double *o = ctx + ((size_t)b * Lq + i) * D + (size_t)hh * d;
-            bad += attend_row(q, Kh, D, Vh, D, Lk, d, sc, i, mask_kind, len_b, wrow, o);
+            bad += attend_row(q, Kh, D, Vh, D, Lk, d, sc, i, mask_kind, len_b, NULL, wrow, o);
         }
         free(wrow);
     }

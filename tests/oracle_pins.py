@@ -267,6 +267,50 @@ def pin_sdpa_rows_match_full(orc):
         assert np.array_equal(got, full.reshape(-1, d)[rows]), "row sample differs"
 
 
+def pin_printed_mask_as_float_mask(orc):
+    """The printed 4x4 mask given as an additive float mask is the causal mask:
+    the outputs are identical to mask_kind = causal, bit for bit."""
+    mask = read_mask_fixture()
+    rng = _rng(13)
+    Q, K, V = _qkv(rng, 2, 3, 4, 4, 8)
+    a = orc.sdpa(Q, K, V, add_mask=mask)
+    b = orc.sdpa(Q, K, V, mask_kind=MASK_CAUSAL)
+    assert np.array_equal(a, b), "float form of the printed mask differs from causal"
+
+
+def pin_float_mask_torch(orc):
+    """Library cross-check: a float mask with finite values and -inf entries,
+    per head and broadcast, against torch's float64 SDPA attn_mask."""
+    import torch
+    import torch.nn.functional as F
+    rng = _rng(14)
+    for B, H, Lq, Lk, d, per in ((2, 3, 9, 13, 16, "head"), (1, 2, 7, 7, 32, "bcast"),
+                                 (3, 1, 5, 20, 8, "batch")):
+        Q, K, V = _qkv(rng, B, H, Lq, Lk, d)
+        shape = {"head": (B, H, Lq, Lk), "bcast": (Lq, Lk), "batch": (B, 1, Lq, Lk)}[per]
+        m = rng.standard_normal(shape) * 3.0
+        m[rng.random(shape) < 0.3] = -np.inf
+        m[..., 0] = 0.0                      # every row keeps key 0 visible
+        ref = F.scaled_dot_product_attention(
+            torch.from_numpy(Q), torch.from_numpy(K), torch.from_numpy(V),
+            attn_mask=torch.from_numpy(np.broadcast_to(m, (B, H, Lq, Lk)).copy())).numpy()
+        _allclose(orc.sdpa(Q, K, V, add_mask=m), ref, 1e-12, f"float mask {per}")
+
+
+def pin_float_mask_row_shift(orc):
+    """Adding one constant to a whole mask row changes nothing (softmax shift
+    invariance); adding it to one entry does."""
+    rng = _rng(15)
+    Q, K, V = _qkv(rng, 1, 2, 6, 9, 8)
+    m = rng.standard_normal((6, 9))
+    base = orc.sdpa(Q, K, V, add_mask=m)
+    _allclose(orc.sdpa(Q, K, V, add_mask=m + rng.standard_normal((6, 1)) * 4), base,
+              1e-12, "row shift")
+    m2 = m.copy()
+    m2[2, 3] += 2.0
+    assert not np.allclose(orc.sdpa(Q, K, V, add_mask=m2)[0, :, 2], base[0, :, 2])
+
+
 # ----------------------------------------------------------------- MHA pins
 
 def _mha_inputs(rng, B, Lq, Lk, D, cross=True):

@@ -29,6 +29,10 @@ MUTANTS = [
     ("mha_scale_uses_dmodel", "const double sc = 1.0 / sqrt((double)d);\n#ifdef",
      "const double sc = 1.0 / sqrt((double)D);\n#ifdef"),
     ("key_proj_uses_wq", "matmul(x_kv, Wk, Kp,", "matmul(x_kv, Wq, Kp,"),
+    ("float_mask_before_scale", "w[j] = scale * dot + mask_entry(i, j, mask_kind, len_b);\n        if (add_row)\n            w[j] += add_row[j];",
+     "w[j] = scale * (dot + (add_row ? add_row[j] : 0.0)) + mask_entry(i, j, mask_kind, len_b);"),
+    ("float_mask_transposed", "(int64_t)hh * add_stride_h + (int64_t)i * Lk\n                                          : NULL;",
+     "(int64_t)hh * add_stride_h + (int64_t)i\n                                          : NULL;"),
     ("query_row_stride_wrong", "bad += attend_row(Qh + (size_t)i * d,",
      "bad += attend_row(Qh + (size_t)(Lq - 1 - i) * d,"),
 ]
