@@ -224,8 +224,18 @@ def bench_sdpa(args, w, rank, world, local_rank):
     if in_bytes + out_bytes < 2 * L2_BYTES:
         flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
 
+    add_mask = None
+    mask_kind = w.mask
+    if args.float_mask:
+        # the causal mask handed over as an opaque additive float mask [Lq, Lk]
+        if w.mask != 1:
+            raise SystemExit("--float-mask needs a causal workload")
+        add_mask = torch.triu(torch.full((w.Lq, w.Lk), float("-inf"), device=dev), 1)
+        mask_kind = 0
+
     def step():
-        mha.sdpa_forward(Qd, Kd, Vd, mask_kind=w.mask, key_lengths=kl, out=Od)
+        mha.sdpa_forward(Qd, Kd, Vd, mask_kind=mask_kind, key_lengths=kl, out=Od,
+                         add_mask=add_mask)
 
     stream = torch.cuda.current_stream()
     for _ in range(args.warmup):
@@ -407,7 +417,8 @@ def run_gpu(args):
         "dtype": "bf16",
         "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "Lq": w.Lq, "Lk": w.Lk, "d": w.d,
-                   "mask": {0: "none", 1: "causal", 2: "key_padding", 3: "causal+key_padding"}[w.mask],
+                   "mask": ({0: "none", 1: "causal", 2: "key_padding", 3: "causal+key_padding"}[w.mask]
+                            + (" (as additive float mask [Lq, Lk])" if args.float_mask else "")),
                    "flops_per_step": w.flops(r["lens"]), "l2": r["l2"],
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "pct_bf16_peak_nominal": round(100.0 * ach / NOMINAL_BF16_TFLOPS, 2),
@@ -474,6 +485,8 @@ def main(argv=None):
                     help="override the sequence length (profiling captures)")
     ap.add_argument("--heads", type=int, default=None,
                     help="override the head count (profiling captures)")
+    ap.add_argument("--float-mask", action="store_true",
+                    help="pass the causal mask as an additive float mask [Lq, Lk]")
     ap.add_argument("--skip-mha", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--cpu-rows-per-head", type=int, default=None,

@@ -92,6 +92,30 @@ mha_status sdpa_forward(const void *Q, const void *K, const void *V, void *O,
                         mha_stream stream);
 
 /*
+ * sdpa_forward_float_mask -- sdpa_forward with an additive float mask added
+ * to the scaled scores, the optional mask of the reference SDPA that "The
+ * Transformer" (rayaq.ca) describes in "Attention, by hand" (with -inf
+ * giving weight exactly 0, "Masks: who may look at whom").
+ *   add_mask : device float32; element (b, h, i, j) at
+ *              add_mask[b*mask_stride_b + h*mask_stride_h + i*Lk + j]
+ *              (strides in elements, >= 0; 0 broadcasts over that axis;
+ *              rows of Lk contiguous values).  Entries must be finite or
+ *              -inf.  4-byte aligned.
+ *   Other arguments, layouts and support as for sdpa_forward; mask_kind and
+ *   key_lengths still apply on top.  A query row whose keys are all blocked
+ *   has no defined softmax and is written as zeros.
+ * Returns MHA_OK, MHA_ERR_INVALID_ARG, MHA_ERR_UNSUPPORTED or MHA_ERR_CUDA.
+ */
+mha_status sdpa_forward_float_mask(const void *Q, const void *K, const void *V,
+                                   void *O, int B, int H, int Lq, int Lk,
+                                   int d, float scale, int mask_kind,
+                                   const int32_t *key_lengths,
+                                   const float *add_mask,
+                                   int64_t mask_stride_b,
+                                   int64_t mask_stride_h, mha_dtype in_dtype,
+                                   mha_dtype out_dtype, mha_stream stream);
+
+/*
  * mha_create -- allocate a multi-head attention layer handle.
  *   d_model   : model width D.
  *   dtype     : element type of x, W and out (MHA_BF16 or MHA_F32).

@@ -47,6 +47,10 @@ def _declare(lib):
     lib.sdpa_forward.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, i32, vp,
                                  i32, i32, vp]
     lib.sdpa_forward.restype = i32
+    i64 = ctypes.c_int64
+    lib.sdpa_forward_float_mask.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, i32,
+                                            vp, vp, i64, i64, i32, i32, vp]
+    lib.sdpa_forward_float_mask.restype = i32
     lib.mha_create.argtypes = [ctypes.POINTER(vp), i32, i32, i32, i32, i32]
     lib.mha_create.restype = i32
     lib.mha_forward.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp]
@@ -109,10 +113,31 @@ def _stream(stream) -> ctypes.c_void_p:
     return ctypes.c_void_p(s.cuda_stream)
 
 
+def _mask_strides(add_mask, B, H, Lq, Lk):
+    """Batch and head strides (elements, 0 = broadcast) of a float32 mask
+    broadcastable to [B, H, Lq, Lk] whose [Lq, Lk] rows are contiguous."""
+    if add_mask.dtype != torch.float32 or not add_mask.is_cuda:
+        raise ValueError("add_mask must be a float32 CUDA tensor")
+    m = add_mask
+    while m.dim() < 4:
+        m = m.unsqueeze(0)
+    if m.dim() != 4 or tuple(m.shape[2:]) != (Lq, Lk) or m.shape[0] not in (1, B) \
+            or m.shape[1] not in (1, H):
+        raise ValueError("add_mask must broadcast to [B, H, Lq, Lk]")
+    if Lk > 1 and m.stride(3) != 1 or Lq > 1 and m.stride(2) != Lk:
+        raise ValueError("add_mask rows must be contiguous")
+    sb = m.stride(0) if m.shape[0] > 1 else 0
+    sh = m.stride(1) if m.shape[1] > 1 else 0
+    return sb, sh
+
+
 def sdpa_forward(Q, K, V, scale: float | None = None, mask_kind: int = MASK_NONE,
                  key_lengths=None, out_dtype: torch.dtype | None = None, out=None,
-                 stream=None):
-    """O = softmax(Q K^T * scale + mask) V for Q [B,H,Lq,d], K/V [B,H,Lk,d]."""
+                 stream=None, add_mask=None):
+    """O = softmax(Q K^T * scale + mask) V for Q [B,H,Lq,d], K/V [B,H,Lk,d].
+
+    ``add_mask``: optional float32 tensor broadcastable to [B,H,Lq,Lk], added
+    to the scaled scores (-inf blocks a key)."""
     B, H, Lq, d = Q.shape
     Lk = K.shape[2]
     if K.shape != (B, H, Lk, d) or V.shape != (B, H, Lk, d):
@@ -126,6 +151,15 @@ def sdpa_forward(Q, K, V, scale: float | None = None, mask_kind: int = MASK_NONE
         raise ValueError("out has the wrong shape or dtype")
     if key_lengths is not None and key_lengths.dtype != torch.int32:
         raise ValueError("key_lengths must be int32")
+    if add_mask is not None:
+        sb, sh = _mask_strides(add_mask, B, H, Lq, Lk)
+        st = lib().sdpa_forward_float_mask(
+            _dev_ptr(Q), _dev_ptr(K), _dev_ptr(V), _dev_ptr(out), B, H, Lq, Lk, d,
+            float(scale or 0.0), int(mask_kind), _dev_ptr(key_lengths),
+            ctypes.c_void_p(add_mask.data_ptr()), sb, sh, _dtype_code(Q.dtype),
+            _dtype_code(odt), _stream(stream))
+        _check(st, "sdpa_forward_float_mask")
+        return out
     st = lib().sdpa_forward(_dev_ptr(Q), _dev_ptr(K), _dev_ptr(V), _dev_ptr(out), B, H, Lq, Lk,
                             d, float(scale or 0.0), int(mask_kind), _dev_ptr(key_lengths),
                             _dtype_code(Q.dtype), _dtype_code(odt), _stream(stream))

@@ -33,6 +33,8 @@ struct SdpaF32Params {
   int mask_kind;
   float scale;
   int ctx_layout;
+  const float* add_mask;  // optional additive float mask (scaled-score units)
+  int64_t mask_sb, mask_sh;
 };
 
 __device__ __forceinline__ float warp_max(float v) {
@@ -123,6 +125,10 @@ __global__ void __launch_bounds__(kWarps * 32) sdpa_f32_kernel(const SdpaF32Para
         const int key = k0 + lane + 32 * t;
         const bool valid = key < key_end && (!causal || key <= q_row);
         s[i][t] = valid ? s[i][t] : -INFINITY;
+        if (p.add_mask && valid && q_row < p.Lq)
+          s[i][t] += __ldg(p.add_mask + static_cast<int64_t>(b) * p.mask_sb +
+                           static_cast<int64_t>(h) * p.mask_sh +
+                           static_cast<int64_t>(q_row) * p.Lk + key);
       }
       const float m_new = fmaxf(m[i], warp_max(fmaxf(s[i][0], s[i][1])));
       if (m_new == -INFINITY) {  // nothing visible to this row yet (uniform in the warp)
@@ -322,6 +328,9 @@ cudaError_t launch_sdpa_f32(const SdpaArgs& a, const DeviceCtl& ctl) {
   p.mask_kind = a.mask_kind;
   p.scale = a.scale;
   p.ctx_layout = a.ctx_layout ? 1 : 0;
+  p.add_mask = a.add_mask;
+  p.mask_sb = a.mask_sb;
+  p.mask_sh = a.mask_sh;
   if (a.Lq == 0 || a.H == 0 || a.B == 0) return cudaSuccess;
   const dim3 grid((a.Lq + kRowsC - 1) / kRowsC, a.H, a.B);
   auto smem = [](int DP) { return (kRowsC * DP + kKeys * (DP + 1) + kKeys * DP) * 4; };

@@ -22,6 +22,10 @@ struct SdpaArgs {
   mha_dtype in_dtype, out_dtype;
   bool ctx_layout;
   cudaStream_t stream;
+  // optional additive float mask: element (b, h, i, j) at
+  // add_mask[b*mask_sb + h*mask_sh + i*Lk + j]; nullptr when absent
+  const float* add_mask;
+  int64_t mask_sb, mask_sh;
 };
 
 // Row-major GEMM C = A[M,K] @ W[K,N] with a choice of store layout.

@@ -195,6 +195,27 @@ mha_status sdpa_forward(const void* Q, const void* K, const void* V, void* O, in
   return from_cuda(e);
 }
 
+mha_status sdpa_forward_float_mask(const void* Q, const void* K, const void* V, void* O, int B,
+                                   int H, int Lq, int Lk, int d, float scale, int mask_kind,
+                                   const int32_t* key_lengths, const float* add_mask,
+                                   int64_t mask_stride_b, int64_t mask_stride_h,
+                                   mha_dtype in_dtype, mha_dtype out_dtype, mha_stream stream) {
+  const mha_status st = check_sdpa(Q, K, V, O, B, H, Lq, Lk, d, scale, mask_kind, key_lengths,
+                                   in_dtype, out_dtype);
+  if (st != MHA_OK) return st;
+  if (mask_stride_b < 0 || mask_stride_h < 0) return MHA_ERR_INVALID_ARG;
+  if (static_cast<long long>(B) * H * Lq == 0) return MHA_OK;
+  if (!add_mask || (reinterpret_cast<uintptr_t>(add_mask) & 3u)) return MHA_ERR_INVALID_ARG;
+  DeviceCtl ctl;
+  if (!get_device_ctl(&ctl)) return MHA_ERR_CUDA;
+  SdpaArgs a{Q, K, V, O, B, H, Lq, Lk, d,
+             scale == 0.f ? static_cast<float>(1.0 / sqrt(static_cast<double>(d))) : scale,
+             mask_kind, key_lengths, in_dtype, out_dtype, false,
+             reinterpret_cast<cudaStream_t>(stream), add_mask, mask_stride_b, mask_stride_h};
+  const cudaError_t e = in_dtype == MHA_BF16 ? launch_sdpa_bf16(a, ctl) : launch_sdpa_f32(a, ctl);
+  return from_cuda(e);
+}
+
 mha_status mha_create(mha_handle* out, int d_model, mha_dtype dtype, int max_batch, int max_lq,
                       int max_lk) {
   if (!out) return MHA_ERR_INVALID_ARG;

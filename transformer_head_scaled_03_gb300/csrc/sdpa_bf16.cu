@@ -52,6 +52,10 @@ struct SdpaParams {
   float scale_log2;  // scale * log2(e)
   int out_f32;
   int ctx_layout;
+  const float* add_mask;  // additive float mask (kernels instantiated with kAddMask)
+  int64_t mask_sb, mask_sh;
+  float inv_scale;        // the mask is added to raw scores as M / scale
+  int mask_vec;           // rows are 16-byte aligned: load the mask as float4
 };
 
 template <int D, int NQT, int NST>
@@ -99,7 +103,7 @@ __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, uint64
   }
 }
 
-template <int D, int NQT, int NST>
+template <int D, int NQT, int NST, bool kAddMask>
 __global__ void __launch_bounds__(Cfg<D, NQT, NST>::kThreads, 1)
     sdpa_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ,
                          const __grid_constant__ CUtensorMap tmK,
@@ -322,6 +326,29 @@ __global__ void __launch_bounds__(Cfg<D, NQT, NST>::kThreads, 1)
 #pragma unroll
           for (int c = 0; c < 128; ++c) x[c] = c <= last ? x[c] : -INFINITY;
         }
+        if constexpr (kAddMask) {
+          // additive float mask, in raw-score units (M / scale); -inf blocks
+          if (q_row < p.Lq) {
+            const float* mrow = p.add_mask + static_cast<int64_t>(b) * p.mask_sb +
+                                static_cast<int64_t>(h) * p.mask_sh +
+                                static_cast<int64_t>(q_row) * p.Lk + k0;
+            const int nvalid = min(kBlockN, p.Lk - k0);
+            if (p.mask_vec && nvalid == kBlockN) {
+#pragma unroll
+              for (int c = 0; c < 128; c += 4) {
+                const float4 mv = __ldg(reinterpret_cast<const float4*>(mrow + c));
+                x[c] = fmaf(mv.x, p.inv_scale, x[c]);
+                x[c + 1] = fmaf(mv.y, p.inv_scale, x[c + 1]);
+                x[c + 2] = fmaf(mv.z, p.inv_scale, x[c + 2]);
+                x[c + 3] = fmaf(mv.w, p.inv_scale, x[c + 3]);
+              }
+            } else {
+#pragma unroll
+              for (int c = 0; c < 128; ++c)
+                if (c < nvalid) x[c] = fmaf(__ldg(mrow + c), p.inv_scale, x[c]);
+            }
+          }
+        }
       };
       // tile maximum: eight independent 3-input max chains, then combine
       auto tile_max = [&](const float (&x)[128]) -> float {
@@ -443,7 +470,7 @@ __global__ void __launch_bounds__(Cfg<D, NQT, NST>::kThreads, 1)
   if (warp == C::kMmaWarp) tmem_dealloc<C::kTmemCols>(tmem);
 }
 
-template <int D, int NQT, int NST>
+template <int D, int NQT, int NST, bool kAddMask>
 cudaError_t launch_impl(const SdpaArgs& a, const DeviceCtl& ctl) {
   using C = Cfg<D, NQT, NST>;
   CUtensorMap maps[3];
@@ -474,10 +501,16 @@ cudaError_t launch_impl(const SdpaArgs& a, const DeviceCtl& ctl) {
   p.scale_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
   p.out_f32 = a.out_dtype == MHA_F32 ? 1 : 0;
   p.ctx_layout = a.ctx_layout ? 1 : 0;
+  p.add_mask = a.add_mask;
+  p.mask_sb = a.mask_sb;
+  p.mask_sh = a.mask_sh;
+  p.inv_scale = 1.f / a.scale;
+  p.mask_vec = a.add_mask && (reinterpret_cast<uintptr_t>(a.add_mask) & 15u) == 0 &&
+               a.Lk % 4 == 0 && a.mask_sb % 4 == 0 && a.mask_sh % 4 == 0;
   const long long grid = static_cast<long long>(p.num_q_blocks) * a.B * a.H;
   if (grid <= 0) return cudaSuccess;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  auto kern = sdpa_fwd_bf16_kernel<D, NQT, NST>;
+  auto kern = sdpa_fwd_bf16_kernel<D, NQT, NST, kAddMask>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
@@ -493,8 +526,17 @@ cudaError_t launch_sdpa_bf16(const SdpaArgs& a, const DeviceCtl& ctl) {
   // Two query tiles per CTA share every K/V tile (half the K/V traffic per
   // query row); a single tile when there are too few rows to fill two.
   const bool two = a.Lq > kBlockM;
-  if (a.d == 64) return two ? launch_impl<64, 2, 3>(a, ctl) : launch_impl<64, 1, 3>(a, ctl);
-  if (a.d == 128) return two ? launch_impl<128, 2, 2>(a, ctl) : launch_impl<128, 1, 2>(a, ctl);
+  if (a.add_mask) {
+    if (a.d == 64)
+      return two ? launch_impl<64, 2, 3, true>(a, ctl) : launch_impl<64, 1, 3, true>(a, ctl);
+    if (a.d == 128)
+      return two ? launch_impl<128, 2, 2, true>(a, ctl) : launch_impl<128, 1, 2, true>(a, ctl);
+    return cudaErrorInvalidValue;
+  }
+  if (a.d == 64)
+    return two ? launch_impl<64, 2, 3, false>(a, ctl) : launch_impl<64, 1, 3, false>(a, ctl);
+  if (a.d == 128)
+    return two ? launch_impl<128, 2, 2, false>(a, ctl) : launch_impl<128, 1, 2, false>(a, ctl);
   return cudaErrorInvalidValue;
 }
 
