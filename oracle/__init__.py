@@ -61,6 +61,11 @@ def _declare(lib):
     lib.oracle_mha.argtypes = [dp, dp, dp, dp, dp, dp, dp, c_int, c_int, c_int,
                                c_int, c_int, c_int, ip, c_int]
     lib.oracle_mha.restype = c_int
+    lib.oracle_encoder_layer.argtypes = [dp] * 17 + [c_double, dp, c_int, c_int, c_int, c_int,
+                                                     c_int, c_int, ip, c_int]
+    lib.oracle_encoder_layer.restype = c_int
+    lib.oracle_encoder_layer_num_params.argtypes = [c_int, c_int]
+    lib.oracle_encoder_layer_num_params.restype = ctypes.c_long
     lib.oracle_num_threads.argtypes = []
     lib.oracle_num_threads.restype = c_int
     return lib
@@ -185,6 +190,37 @@ class Oracle:
         self.last_bad_rows = int(bad)
         return out
 
+
+ENCODER_PARAM_NAMES = ("Wq", "Wk", "Wv", "Wo", "bq", "bk", "bv", "bo", "ln1_gamma",
+                       "ln1_beta", "W1", "b1", "W2", "b2", "ln2_gamma", "ln2_beta")
+
+
+def _encoder_layer(self, x, params: dict, h: int, eps: float = 1e-5,
+                   mask_kind: int = MASK_NONE, key_lengths=None, nthreads: int = 0):
+    """Post-norm encoder layer: x [B,L,D] and the parameters (names in
+    ENCODER_PARAM_NAMES; W* [D,D], W1 [D,F], W2 [F,D], vectors 1-D) -> [B,L,D]."""
+    x = _d(x)
+    B, L, D = x.shape
+    arrs = [_d(params[n]) for n in ENCODER_PARAM_NAMES]
+    F = arrs[10].shape[1]
+    out = np.empty((B, L, D))
+    kl, klp = _lengths(mask_kind, key_lengths, B)
+    # parameter pointers in ENCODER_PARAM_NAMES order = the C argument order
+    bad = self.lib.oracle_encoder_layer(_ptr(x), *[_ptr(a) for a in arrs], float(eps),
+                                        _ptr(out), B, L, D, int(h), F, int(mask_kind), klp,
+                                        int(nthreads))
+    if bad < 0:
+        raise ValueError("d_model must be divisible by the number of heads")
+    self.last_bad_rows = int(bad)
+    return out
+
+
+def _encoder_num_params(self, D: int, F: int) -> int:
+    return int(self.lib.oracle_encoder_layer_num_params(D, F))
+
+
+Oracle.encoder_layer = _encoder_layer
+Oracle.encoder_num_params = _encoder_num_params
 
 _default = None
 

@@ -280,6 +280,141 @@ int oracle_mha(const double *x_q, const double *x_kv, const double *Wq,
     return bad;
 }
 
+/* Y[M, N] = X[M, Kd] @ W[Kd, N] + bias[N] (bias may be NULL). */
+static void matmul_bias(const double *X, const double *Wt, const double *bias, double *Y,
+                        long M, int Kd, int N)
+{
+    matmul(X, Wt, Y, M, Kd, N);
+    if (!bias)
+        return;
+#pragma omp parallel for schedule(static)
+    for (long m = 0; m < M; ++m)
+        for (int n = 0; n < N; ++n)
+            Y[(size_t)m * N + n] += bias[n];
+}
+
+/*
+ * LayerNorm of every row of R = A + B ([M, D] each), in place into Y:
+ *   Y[m, :] = (R[m, :] - mean) / sqrt(var + eps) * gamma + beta,
+ * mean and var (population variance, divisor D) over the row's D values.
+ *   -- "The Transformer" (rayaq.ca), "Residuals and LayerNorm": each
+ *      position's values are rescaled to mean 0 and variance 1, then a
+ *      learned scale and shift are applied; the residual is added first
+ *      (post-norm, output = LayerNorm(x + Sublayer(x)), hoshank.vercel.app,
+ *      "The Mathematics").
+ */
+static void add_layernorm(const double *A, const double *B, const double *gamma,
+                          const double *beta, double eps, double *Y, long M, int D)
+{
+#pragma omp parallel for schedule(static)
+    for (long m = 0; m < M; ++m) {
+        double mean = 0.0;
+        for (int c = 0; c < D; ++c)
+            mean += A[(size_t)m * D + c] + B[(size_t)m * D + c];
+        mean /= D;
+        double var = 0.0;
+        for (int c = 0; c < D; ++c) {
+            const double r = A[(size_t)m * D + c] + B[(size_t)m * D + c] - mean;
+            var += r * r;
+        }
+        var /= D;
+        const double inv = 1.0 / sqrt(var + eps);
+        for (int c = 0; c < D; ++c) {
+            const double r = A[(size_t)m * D + c] + B[(size_t)m * D + c] - mean;
+            Y[(size_t)m * D + c] = r * inv * gamma[c] + beta[c];
+        }
+    }
+}
+
+/*
+ * One post-norm Transformer encoder layer, forward, no dropout:
+ *   a   = MultiHead(x, x, x) with biases: Q = x Wq + bq, K = x Wk + bk,
+ *         V = x Wv + bv, heads as in oracle_mha, a = Concat(heads) Wo + bo
+ *   x1  = LayerNorm1(x + a)
+ *   f   = max(0, x1 W1 + b1) W2 + b2          (position-wise FFN)
+ *   out = LayerNorm2(x1 + f)
+ *   -- hoshank.vercel.app, "The Mathematics" (FFN and sublayer equations);
+ *      rayaq.ca, "The feed-forward block", "Residuals and LayerNorm", "The
+ *      encoder stack" and the EncoderLayer of "Implementation".
+ * Shapes: x, out [B, L, D]; Wq..Wo [D, D]; b* [D]; W1 [D, F]; b1 [F];
+ * W2 [F, D]; b2 [D]; ln gamma/beta [D].  Returns -1 when D % h != 0, else
+ * the number of query rows with no visible key.
+ */
+int oracle_encoder_layer(const double *x, const double *Wq, const double *Wk,
+                         const double *Wv, const double *Wo, const double *bq,
+                         const double *bk, const double *bv, const double *bo,
+                         const double *g1, const double *be1, const double *W1,
+                         const double *b1, const double *W2, const double *b2,
+                         const double *g2, const double *be2, double eps,
+                         double *out, int B, int L, int D, int h, int F,
+                         int mask_kind, const int32_t *key_lengths, int nthreads)
+{
+    if (h <= 0 || D % h != 0)
+        return -1;
+    const int d = D / h;
+    const double sc = 1.0 / sqrt((double)d);
+    const long M = (long)B * L;
+#ifdef _OPENMP
+    if (nthreads > 0)
+        omp_set_num_threads(nthreads);
+#endif
+    (void)nthreads;
+    double *Qp = (double *)malloc(sizeof(double) * (size_t)M * D + 8);
+    double *Kp = (double *)malloc(sizeof(double) * (size_t)M * D + 8);
+    double *Vp = (double *)malloc(sizeof(double) * (size_t)M * D + 8);
+    double *ctx = (double *)malloc(sizeof(double) * (size_t)M * D + 8);
+    double *a = (double *)malloc(sizeof(double) * (size_t)M * D + 8);
+    double *x1 = (double *)malloc(sizeof(double) * (size_t)M * D + 8);
+    double *hid = (double *)malloc(sizeof(double) * (size_t)M * F + 8);
+    double *f = (double *)malloc(sizeof(double) * (size_t)M * D + 8);
+    matmul_bias(x, Wq, bq, Qp, M, D, D);
+    matmul_bias(x, Wk, bk, Kp, M, D, D);
+    matmul_bias(x, Wv, bv, Vp, M, D, D);
+    int bad = 0;
+#pragma omp parallel for schedule(dynamic) reduction(+ : bad)
+    for (long bh = 0; bh < (long)B * h; ++bh) {
+        const int b = (int)(bh / h);
+        const int hh = (int)(bh % h);
+        const int len_b = len_of(key_lengths, mask_kind, b, L);
+        double *wrow = (double *)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1));
+        for (int i = 0; i < L; ++i) {
+            const double *q = Qp + ((size_t)b * L + i) * D + (size_t)hh * d;
+            const double *Kh = Kp + (size_t)b * L * D + (size_t)hh * d;
+            const double *Vh = Vp + (size_t)b * L * D + (size_t)hh * d;
+            double *o = ctx + ((size_t)b * L + i) * D + (size_t)hh * d;
+            bad += attend_row(q, Kh, D, Vh, D, L, d, sc, i, mask_kind, len_b, NULL, wrow, o);
+        }
+        free(wrow);
+    }
+    matmul_bias(ctx, Wo, bo, a, M, D, D);
+    add_layernorm(x, a, g1, be1, eps, x1, M, D);
+    matmul_bias(x1, W1, b1, hid, M, D, F);
+#pragma omp parallel for schedule(static)
+    for (long i = 0; i < M * F; ++i)
+        hid[i] = hid[i] > 0.0 ? hid[i] : 0.0;
+    matmul_bias(hid, W2, b2, f, M, F, D);
+    add_layernorm(x1, f, g2, be2, eps, out, M, D);
+    free(Qp);
+    free(Kp);
+    free(Vp);
+    free(ctx);
+    free(a);
+    free(x1);
+    free(hid);
+    free(f);
+    return bad;
+}
+
+/* Number of parameters of the encoder layer above (weights, biases and the
+ * two LayerNorms' scale and shift), for d_model D and FFN width F. */
+long oracle_encoder_layer_num_params(int D, int F)
+{
+    return 4L * D * D + 4L * D          /* Wq, Wk, Wv, Wo and their biases */
+           + (long)D * F + F            /* W1, b1 */
+           + (long)F * D + D            /* W2, b2 */
+           + 2L * (D + D);              /* two LayerNorms: gamma, beta */
+}
+
 int oracle_num_threads(void)
 {
 #ifdef _OPENMP

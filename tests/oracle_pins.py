@@ -408,4 +408,107 @@ def pin_mha_linearity(orc):
     _allclose(a, b, 1e-12, "linear in Wv")
 
 
+# --------------------------------------------------------- encoder layer
+
+def read_params_fixture():
+    vals = {}
+    with open(os.path.join(GOLDEN, "encoder_layer_params.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                k, v = line.split()
+                vals[k] = int(v)
+    return vals
+
+
+def _encoder_params(rng, D, F, scale=1.0):
+    p = {}
+    for n in ("Wq", "Wk", "Wv", "Wo"):
+        p[n] = rng.standard_normal((D, D)) / math.sqrt(D)
+    for n in ("bq", "bk", "bv", "bo", "b2", "ln1_beta", "ln2_beta"):
+        p[n] = rng.standard_normal(D) * 0.1 * scale
+    p["b1"] = rng.standard_normal(F) * 0.1 * scale
+    p["W1"] = rng.standard_normal((D, F)) / math.sqrt(D)
+    p["W2"] = rng.standard_normal((F, D)) / math.sqrt(F)
+    p["ln1_gamma"] = 1.0 + rng.standard_normal(D) * 0.1 * scale
+    p["ln2_gamma"] = 1.0 + rng.standard_normal(D) * 0.1 * scale
+    return p
+
+
+def pin_encoder_param_count(orc):
+    """The printed parameter count of the base encoder layer, and the FFN's
+    two-thirds share of it."""
+    g = read_params_fixture()
+    D, F = g["d_model"], g["d_ff"]
+    assert orc.encoder_num_params(D, F) == g["params"]
+    ffn = D * F + F + F * D + D
+    assert abs(ffn / g["params"] - 2.0 / 3.0) < 0.005
+    # and the arrays the layer consumes add up to the same count
+    rng = _rng(30)
+    p = _encoder_params(rng, D, F)
+    assert sum(a.size for a in p.values()) == g["params"]
+
+
+def _torch_encoder(x, p, h, causal=False, lens=None):
+    import torch
+    D = x.shape[-1]
+    F = p["W1"].shape[1]
+    layer = torch.nn.TransformerEncoderLayer(D, h, F, dropout=0.0, activation="relu",
+                                             batch_first=True, norm_first=False,
+                                             dtype=torch.float64)
+    layer.eval()
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a))
+    with torch.no_grad():
+        layer.self_attn.in_proj_weight.copy_(t(np.concatenate([p["Wq"].T, p["Wk"].T, p["Wv"].T])))
+        layer.self_attn.in_proj_bias.copy_(t(np.concatenate([p["bq"], p["bk"], p["bv"]])))
+        layer.self_attn.out_proj.weight.copy_(t(p["Wo"].T))
+        layer.self_attn.out_proj.bias.copy_(t(p["bo"]))
+        layer.linear1.weight.copy_(t(p["W1"].T))
+        layer.linear1.bias.copy_(t(p["b1"]))
+        layer.linear2.weight.copy_(t(p["W2"].T))
+        layer.linear2.bias.copy_(t(p["b2"]))
+        layer.norm1.weight.copy_(t(p["ln1_gamma"]))
+        layer.norm1.bias.copy_(t(p["ln1_beta"]))
+        layer.norm2.weight.copy_(t(p["ln2_gamma"]))
+        layer.norm2.bias.copy_(t(p["ln2_beta"]))
+        L = x.shape[1]
+        mask = torch.triu(torch.full((L, L), float("-inf"), dtype=torch.float64), 1) if causal else None
+        kpm = None
+        if lens is not None:
+            kpm = torch.arange(L)[None, :] >= torch.from_numpy(np.asarray(lens))[:, None]
+        return layer(t(x), src_mask=mask, src_key_padding_mask=kpm).numpy()
+
+
+def pin_encoder_torch(orc):
+    """Library cross-check: torch.nn.TransformerEncoderLayer (post-norm, ReLU,
+    no dropout) in float64 with the same weights (transposed: torch applies
+    x W^T)."""
+    rng = _rng(31)
+    for B, L, D, h, F, mk in ((2, 7, 32, 4, 64, MASK_NONE), (1, 9, 48, 3, 96, MASK_CAUSAL),
+                              (3, 6, 16, 2, 40, MASK_KEY_PADDING)):
+        x = rng.standard_normal((B, L, D))
+        p = _encoder_params(rng, D, F)
+        lens = np.array([6, 2, 4], np.int32) if mk == MASK_KEY_PADDING else None
+        ref = _torch_encoder(x, p, h, causal=mk == MASK_CAUSAL, lens=lens)
+        got = orc.encoder_layer(x, p, h, mask_kind=mk, key_lengths=lens)
+        _allclose(got, ref, 1e-10, f"torch encoder layer {B, L, D, h, F, mk}")
+
+
+def pin_encoder_layernorm_rows(orc):
+    """With gamma = 1 and beta = 0 every output row has mean 0 and variance 1
+    (up to eps), and the layer is permutation-equivariant over positions."""
+    rng = _rng(32)
+    B, L, D, h, F = 2, 8, 32, 4, 64
+    x = rng.standard_normal((B, L, D)) * 3
+    p = _encoder_params(rng, D, F)
+    p["ln2_gamma"] = np.ones(D)
+    p["ln2_beta"] = np.zeros(D)
+    y = orc.encoder_layer(x, p, h, eps=0.0)
+    _allclose(y.mean(-1), np.zeros((B, L)), 1e-12, "row means")
+    _allclose(y.var(-1), np.ones((B, L)), 1e-10, "row variances")
+    perm = rng.permutation(L)
+    _allclose(orc.encoder_layer(x[:, perm], p, h), orc.encoder_layer(x, p, h)[:, perm], 1e-11,
+              "permutation equivariance")
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

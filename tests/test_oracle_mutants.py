@@ -33,6 +33,10 @@ MUTANTS = [
      "w[j] = scale * (dot + (add_row ? add_row[j] : 0.0)) + mask_entry(i, j, mask_kind, len_b);"),
     ("float_mask_transposed", "(int64_t)hh * add_stride_h + (int64_t)i * Lk\n                                          : NULL;",
      "(int64_t)hh * add_stride_h + (int64_t)i\n                                          : NULL;"),
+    ("layernorm_unbiased_var", "        var /= D;\n", "        var /= (D - 1);\n"),
+    ("ffn_no_relu", "hid[i] = hid[i] > 0.0 ? hid[i] : 0.0;", "hid[i] = hid[i];"),
+    ("encoder_prenorm_residual", "add_layernorm(x1, f, g2, be2, eps, out, M, D);",
+     "add_layernorm(x, f, g2, be2, eps, out, M, D);"),
     ("query_row_stride_wrong", "bad += attend_row(Qh + (size_t)i * d,",
      "bad += attend_row(Qh + (size_t)(Lq - 1 - i) * d,"),
 ]
