@@ -15,6 +15,10 @@ Extra legs in the same JSON line:
                stores, attention with the concat store, output projection)
                in tokens/s, on the same shape (D = 4096, h = 32) and on the
                base fp32 shape (B1 L128 D512 h8)
+  encoder_layer one post-norm encoder layer (attention with biases,
+               residual + LayerNorm, ReLU FFN d_ff = 4D, residual +
+               LayerNorm) in tokens/s, on the key-padding encoder shape
+               (B32 L512 D512 h8, bf16) and the base fp32 shape (B1 L128)
   cpu_baseline the fp64 oracle on this host's cores on a bounded row sample
 
 Multi-GPU: the path has no exchange step, so N ranks run N replicas (one per
@@ -312,36 +316,10 @@ def bench_mha_layer(w_shape, dtype_name, steps, warmup, local_rank, seed_w=None)
     out = torch.empty_like(x)
     handle = mha.mha_create(D, dtype, B, L, L)
     try:
-        def step():
-            mha.mha_forward(handle, x, x, *Ws, h=h, out=out)
-
-        def timed(fn, n):
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record()
-            for _ in range(n):
-                fn()
-            e1.record()
-            torch.cuda.synchronize()
-            return e0.elapsed_time(e1) / n
-
-        for _ in range(warmup):
-            step()
-        torch.cuda.synchronize()
-        eager_ms = timed(step, steps)
-        # the same call captured once in a CUDA graph and replayed: the
-        # library's device time without the per-call host overhead
-        graph = torch.cuda.CUDAGraph()
-        side = torch.cuda.Stream()
-        side.wait_stream(torch.cuda.current_stream())
-        with torch.cuda.stream(side):
-            step()
-        torch.cuda.current_stream().wait_stream(side)
-        with torch.cuda.graph(graph):
-            step()
-        for _ in range(warmup):
-            graph.replay()
-        torch.cuda.synchronize()
-        graph_ms = timed(graph.replay, steps)
+        # eager, and the same call captured once in a CUDA graph and replayed:
+        # the library's device time without the per-call host overhead
+        eager_ms, graph_ms = _time_eager_and_graph(
+            lambda: mha.mha_forward(handle, x, x, *Ws, h=h, out=out), steps, warmup)
         st = mha.mha_check(handle)
         if st != mha.MHA_OK:
             raise RuntimeError(mha.status_string(st))
@@ -358,6 +336,90 @@ def bench_mha_layer(w_shape, dtype_name, steps, warmup, local_rank, seed_w=None)
             "eager_tokens_per_s": round(B * L / (eager_ms / 1e3), 1),
             "eager_ms_per_layer": round(eager_ms, 4),
             "gpu_launches_per_layer": 3}
+
+
+def bench_encoder_layer(shape, dtype_name, steps, warmup, local_rank, key_padding=None):
+    """Tokens/s of one encoder_forward (post-norm encoder layer: MHA with
+    biases, residual + LayerNorm, ReLU FFN, residual + LayerNorm)."""
+    import torch
+    import transformer_head_scaled_03_gb300 as mha
+    from transformer_head_scaled_03_gb300.inputs import Draws
+
+    B, L, D, h, F = shape
+    dev = torch.device("cuda", local_rank)
+    dtype = torch.bfloat16 if dtype_name == "bf16" else torch.float32
+    g = Draws(0x5EED0200 + D + F)
+    mk = lambda a: torch.from_numpy(a).to(dtype).to(dev)
+    x = mk(g.normal((B, L, D), dtype=dtype_name))
+    p = {}
+    for n in ("Wq", "Wk", "Wv", "Wo"):
+        p[n] = mk(g.normal((D, D), std=1.0 / math.sqrt(D), dtype=dtype_name))
+    p["W1"] = mk(g.normal((D, F), std=1.0 / math.sqrt(D), dtype=dtype_name))
+    p["W2"] = mk(g.normal((F, D), std=1.0 / math.sqrt(F), dtype=dtype_name))
+    for n in ("bq", "bk", "bv", "bo", "b2", "ln1_beta", "ln2_beta"):
+        p[n] = mk(g.normal((D,), std=0.1, dtype=dtype_name))
+    p["b1"] = mk(g.normal((F,), std=0.1, dtype=dtype_name))
+    for n in ("ln1_gamma", "ln2_gamma"):
+        p[n] = mk(1.0 + g.normal((D,), std=0.1, dtype="f32"))
+    lens = None
+    mask = mha.MASK_NONE
+    if key_padding is not None:
+        lens = torch.from_numpy(g.integers(key_padding[0], key_padding[1], B)).to(dev)
+        mask = mha.MASK_KEY_PADDING
+    out = torch.empty_like(x)
+    layer = mha.EncoderLayer(D, h, F, dtype, B, L)
+    try:
+        eager_ms, graph_ms = _time_eager_and_graph(
+            lambda: layer.forward(x, p, mask_kind=mask, key_lengths=lens, out=out), steps, warmup)
+        st = mha.mha_check()
+        if st != mha.MHA_OK:
+            raise RuntimeError(mha.status_string(st))
+    finally:
+        layer.close()
+    # algorithmic flops: the six GEMMs, plus 4*d per unmasked query/key pair
+    keys = B * L if lens is None else int(lens.sum().item())
+    flops = 8.0 * B * L * D * D + 4.0 * B * L * D * F + 4.0 * L * keys * D
+    return {"shape": {"B": B, "L": L, "D": D, "h": h, "d_ff": F, "dtype": dtype_name,
+                      "mask": "none" if lens is None else
+                      f"key_padding, lengths U[{key_padding[0]}, {key_padding[1]}]"},
+            "tokens_per_s": round(B * L / (graph_ms / 1e3), 1),
+            "ms_per_layer": round(graph_ms, 4),
+            "tflops": round(flops / (graph_ms / 1e3) / 1e12, 2),
+            "timing": "CUDA graph replay of one encoder_forward call",
+            "eager_tokens_per_s": round(B * L / (eager_ms / 1e3), 1),
+            "eager_ms_per_layer": round(eager_ms, 4),
+            "gpu_launches_per_layer": 7}
+
+
+def _time_eager_and_graph(step, steps, warmup):
+    """(eager ms, CUDA-graph-replay ms) per call of ``step``."""
+    import torch
+
+    def timed(fn, n):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(n):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / n
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    eager_ms = timed(step, steps)
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()
+    torch.cuda.current_stream().wait_stream(side)
+    with torch.cuda.graph(graph):
+        step()
+    for _ in range(warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    return eager_ms, timed(graph.replay, steps)
 
 
 def run_gpu(args):
@@ -380,6 +442,13 @@ def run_gpu(args):
         mha_layer = [bench_mha_layer((w.B, w.Lq, w.H * w.d, w.H), "bf16", 3, 3, local_rank),
                      bench_mha_layer((1, 128, 512, 8), "f32", 200, 5, local_rank,
                                      seed_w=WORKLOADS[1].seed)]
+    encoder_layer = None
+    if not args.skip_mha:
+        w2 = WORKLOADS[2]
+        encoder_layer = [
+            bench_encoder_layer((w2.B, w2.Lq, w2.H * w2.d, w2.H, 4 * w2.H * w2.d), "bf16", 20, 3,
+                                local_rank, key_padding=w2.len_range),
+            bench_encoder_layer((1, 128, 512, 8, 2048), "f32", 100, 5, local_rank)]
 
     cpu = None
     if rank == 0 and not args.skip_cpu:
@@ -431,6 +500,7 @@ def run_gpu(args):
         "clocks": r["clocks"],
         "cpu_baseline": cpu,
         "mha_layer": mha_layer,
+        "encoder_layer": encoder_layer,
     }
     print(json.dumps(line), flush=True)
     if world > 1:

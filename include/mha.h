@@ -186,6 +186,58 @@ mha_status mha_forward_noalloc(int d_model, mha_dtype dtype, const void *x_q,
                                mha_stream stream);
 
 /*
+ * One post-norm Transformer encoder layer (next to the attention layer it
+ * contains):
+ *   a   = MultiHead(x, x, x) with biases (as mha_forward, plus bq, bk, bv
+ *         added to the projections and bo to the output projection)
+ *   x1  = LayerNorm(x + a) * ln1_gamma + ln1_beta
+ *   f   = max(0, x1 W1 + b1) W2 + b2
+ *   out = LayerNorm(x1 + f) * ln2_gamma + ln2_beta
+ * LayerNorm over each position's D values, population variance, ln_eps
+ * added to the variance (PyTorch's default is 1e-5).
+ *   -- "The Transformer" (hoshank.vercel.app), "The Mathematics" (FFN and
+ *      output = LayerNorm(x + Sublayer(x))); "The Transformer" (rayaq.ca),
+ *      "The feed-forward block", "Residuals and LayerNorm", "The encoder
+ *      stack" and the EncoderLayer of "Implementation".
+ * All parameters have the layer's element type and are device pointers,
+ * 16-byte aligned; matrices are row-major [d_in, d_out] applied as y = x@W.
+ */
+typedef struct {
+    const void *Wq, *Wk, *Wv, *Wo;     /* [D, D] */
+    const void *bq, *bk, *bv, *bo;     /* [D] */
+    const void *ln1_gamma, *ln1_beta;  /* [D] */
+    const void *W1;                    /* [D, F] */
+    const void *b1;                    /* [F] */
+    const void *W2;                    /* [F, D] */
+    const void *b2;                    /* [D] */
+    const void *ln2_gamma, *ln2_beta;  /* [D] */
+} mha_encoder_params;
+
+typedef struct mha_encoder_ctx *mha_encoder;
+
+/* encoder_create -- a layer handle for d_model D, `heads`, FFN width d_ff,
+ * element type `dtype`, up to max_batch x max_len tokens; owns cudaMalloc'd
+ * workspace (Q, K, V, context, two [B,L,D] temporaries, x1, the [B,L,F]
+ * hidden activation).  Supported: BF16 with D/heads in {64, 128} and D, d_ff
+ * multiples of 64; F32 with D/heads <= 128; D <= 4096.  Returns MHA_OK,
+ * MHA_ERR_INVALID_ARG, MHA_ERR_UNSUPPORTED, MHA_ERR_OOM or MHA_ERR_CUDA. */
+mha_status encoder_create(mha_encoder *out, int d_model, int heads, int d_ff,
+                          mha_dtype dtype, int max_batch, int max_len);
+
+/* encoder_forward -- out [B, L, D] = layer(x [B, L, D]); mask_kind and
+ * key_lengths as for mha_forward (self-attention, Lq = Lk = L).  Seven
+ * launches on `stream`.  out must not alias x.  Returns MHA_OK,
+ * MHA_ERR_INVALID_ARG or MHA_ERR_CUDA. */
+mha_status encoder_forward(mha_encoder enc, const void *x,
+                           const mha_encoder_params *params, int B, int L,
+                           int mask_kind, const int32_t *key_lengths,
+                           float ln_eps, void *out, mha_stream stream);
+
+/* encoder_destroy -- free the handle (synchronises the device).  NULL is
+ * accepted. */
+mha_status encoder_destroy(mha_encoder enc);
+
+/*
  * mha_check -- synchronise the current device and report (then clear) its
  * device-side error word.  `handle` may be NULL.  Returns MHA_OK,
  * MHA_ERR_TIMEOUT, MHA_ERR_DEVICE or MHA_ERR_CUDA.

@@ -242,3 +242,7 @@ def sdpa_rows(*a, **k):
 
 def mha(*a, **k):
     return default().mha(*a, **k)
+
+
+def encoder_layer(*a, **k):
+    return default().encoder_layer(*a, **k)

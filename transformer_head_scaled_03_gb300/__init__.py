@@ -11,7 +11,8 @@ importing the package (e.g. for ``inputs``) needs neither torch nor a GPU.
 """
 _BINDING_NAMES = {
     "sdpa_forward", "sdpa_forward_host", "mha_create", "mha_forward", "mha_check",
-    "mha_destroy", "MhaHandle", "MhaError", "set_wait_limit_ms", "selftest_wait_timeout", "status_string", "lib",
+    "mha_destroy", "MhaHandle", "MhaError", "EncoderLayer", "EncoderParams",
+    "ENCODER_PARAM_NAMES", "set_wait_limit_ms", "selftest_wait_timeout", "status_string", "lib",
     "MASK_NONE", "MASK_CAUSAL", "MASK_KEY_PADDING", "MHA_OK", "MHA_ERR_INVALID_ARG",
     "MHA_ERR_UNSUPPORTED", "MHA_ERR_CUDA", "MHA_ERR_OOM", "MHA_ERR_TIMEOUT",
     "MHA_ERR_DEVICE", "MHA_F32", "MHA_BF16", "LIB_PATH",

@@ -36,6 +36,15 @@ _lock = threading.Lock()
 _lib = None
 
 
+ENCODER_PARAM_NAMES = ("Wq", "Wk", "Wv", "Wo", "bq", "bk", "bv", "bo", "ln1_gamma",
+                       "ln1_beta", "W1", "b1", "W2", "b2", "ln2_gamma", "ln2_beta")
+
+
+class EncoderParams(ctypes.Structure):
+    """mha_encoder_params of include/mha.h (device pointers)."""
+    _fields_ = [(n, ctypes.c_void_p) for n in ENCODER_PARAM_NAMES]
+
+
 class MhaError(RuntimeError):
     def __init__(self, status: int, what: str):
         self.status = status
@@ -51,6 +60,13 @@ def _declare(lib):
     lib.sdpa_forward_float_mask.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, i32,
                                             vp, vp, i64, i64, i32, i32, vp]
     lib.sdpa_forward_float_mask.restype = i32
+    lib.encoder_create.argtypes = [ctypes.POINTER(vp), i32, i32, i32, i32, i32, i32]
+    lib.encoder_create.restype = i32
+    lib.encoder_forward.argtypes = [vp, vp, ctypes.POINTER(EncoderParams), i32, i32, i32, vp,
+                                    f32, vp, vp]
+    lib.encoder_forward.restype = i32
+    lib.encoder_destroy.argtypes = [vp]
+    lib.encoder_destroy.restype = i32
     lib.mha_create.argtypes = [ctypes.POINTER(vp), i32, i32, i32, i32, i32]
     lib.mha_create.restype = i32
     lib.mha_forward.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp]
@@ -219,6 +235,53 @@ def mha_forward(handle: MhaHandle, x_q, x_kv, Wq, Wk, Wv, Wo, h: int,
                            _stream(stream))
     _check(st, "mha_forward")
     return out
+
+
+class EncoderLayer:
+    """One post-norm encoder layer on the library (encoder_create /
+    encoder_forward / encoder_destroy).  ``params`` maps the names in
+    ENCODER_PARAM_NAMES to device tensors of the layer's dtype."""
+
+    def __init__(self, d_model: int, heads: int, d_ff: int, dtype: torch.dtype,
+                 max_batch: int, max_len: int):
+        h = ctypes.c_void_p()
+        _check(lib().encoder_create(ctypes.byref(h), d_model, heads, d_ff, _dtype_code(dtype),
+                                    max_batch, max_len), "encoder_create")
+        self._h = h
+        self.d_model, self.heads, self.d_ff, self.dtype = d_model, heads, d_ff, dtype
+
+    def forward(self, x, params: dict, mask_kind: int = MASK_NONE, key_lengths=None,
+                ln_eps: float = 1e-5, out=None, stream=None):
+        if self._h is None:
+            raise RuntimeError("encoder destroyed")
+        B, L, D = x.shape
+        if D != self.d_model or x.dtype != self.dtype:
+            raise ValueError("x does not match the layer")
+        shapes = {"W1": (D, self.d_ff), "b1": (self.d_ff,), "W2": (self.d_ff, D)}
+        for n in ENCODER_PARAM_NAMES:
+            t = params[n]
+            want = shapes.get(n, (D, D) if n.startswith("W") else (D,))
+            if tuple(t.shape) != want or t.dtype != self.dtype:
+                raise ValueError(f"parameter {n} must be {want} {self.dtype}")
+        p = EncoderParams(*[_dev_ptr(params[n]) for n in ENCODER_PARAM_NAMES])
+        if out is None:
+            out = torch.empty_like(x)
+        st = lib().encoder_forward(self._h, _dev_ptr(x), ctypes.byref(p), B, L, int(mask_kind),
+                                   _dev_ptr(key_lengths), float(ln_eps), _dev_ptr(out),
+                                   _stream(stream))
+        _check(st, "encoder_forward")
+        return out
+
+    def close(self):
+        if self._h is not None:
+            _check(lib().encoder_destroy(self._h), "encoder_destroy")
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def mha_check(handle: MhaHandle | None = None) -> int:

@@ -188,6 +188,8 @@ struct GemmF32Params {
   const float* A[3];
   const float* W[3];
   float* C[3];
+  const float* bias[3];
+  int relu[3];
   int store[3];
   int L[3];
   int dh[3];
@@ -289,6 +291,8 @@ __global__ void __launch_bounds__(256) gemm_f32_kernel(const GemmF32Params p) {
   }
   float* C = p.C[z];
   const bool split = p.store[z] == static_cast<int>(GemmStore::kHeadSplit);
+  const float* bias = p.bias[z];
+  const bool relu = p.relu[z] != 0;
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
     const int m = m0 + 2 * ty + i;
@@ -305,7 +309,10 @@ __global__ void __launch_bounds__(256) gemm_f32_kernel(const GemmF32Params p) {
       } else {
         off = static_cast<size_t>(m) * N + n;
       }
-      C[off] = acc[i][j];
+      float v = acc[i][j];
+      if (bias) v += bias[n];
+      if (relu) v = fmaxf(v, 0.f);
+      C[off] = v;
     }
   }
 }
@@ -353,6 +360,8 @@ cudaError_t launch_gemm_f32(const GemmArgs& g, const DeviceCtl&) {
     p.A[i] = static_cast<const float*>(g.prob[i].A);
     p.W[i] = static_cast<const float*>(g.prob[i].W);
     p.C[i] = static_cast<float*>(g.prob[i].C);
+    p.bias[i] = static_cast<const float*>(g.prob[i].bias);
+    p.relu[i] = g.prob[i].relu;
     p.store[i] = static_cast<int>(g.prob[i].store);
     p.L[i] = g.prob[i].L;
     p.dh[i] = g.prob[i].dh;

@@ -45,6 +45,8 @@ static_assert(kSmemBytes <= 232448, "shared memory");
 
 struct GemmParams {
   void* C[3];
+  const __nv_bfloat16* bias[3];
+  int relu[3];
   int store[3];
   int L[3];
   int dh[3];
@@ -157,6 +159,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok) tc_fence_after();
     const int store = p.store[z];
     const int L = p.L[z], dh = p.dh[z];
+    const __nv_bfloat16* bias = p.bias[z];
+    const int relu = p.relu[z];
     __nv_bfloat16* C = static_cast<__nv_bfloat16*>(p.C[z]);
     const uint32_t tbase = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     for (int cb = 0; cb < kBN / 32; ++cb) {
@@ -169,6 +173,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else {
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = 0u;
+      }
+      if (bias) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          v[i] = __float_as_uint(__uint_as_float(v[i]) + __bfloat162float(bias[n + i]));
+      }
+      if (relu) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(fmaxf(__uint_as_float(v[i]), 0.f));
       }
       if (m < p.M) {
         size_t off;
@@ -218,6 +231,8 @@ cudaError_t launch_gemm_bf16(const GemmArgs& g, const DeviceCtl& ctl) {
                            wdims, wstr, wbox, CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
     p.C[i] = pr.C;
+    p.bias[i] = static_cast<const __nv_bfloat16*>(pr.bias);
+    p.relu[i] = pr.relu;
     p.store[i] = static_cast<int>(pr.store);
     p.L[i] = pr.L > 0 ? pr.L : 1;
     p.dh[i] = pr.dh > 0 ? pr.dh : 1;

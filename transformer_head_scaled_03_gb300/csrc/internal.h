@@ -41,6 +41,8 @@ struct GemmProblem {
   GemmStore store;
   int L;   // rows per batch item (head split)
   int dh;  // head width (head split)
+  const void* bias = nullptr;  // [N], same element type, added in the epilogue
+  int relu = 0;                // max(0, .) after the bias
 };
 
 struct GemmArgs {
@@ -55,6 +57,12 @@ struct DeviceCtl {
   unsigned* err;       // device error word
   uint64_t limit_ns;   // wait limit for pipelined kernels
 };
+
+// out[m, :] = LayerNorm(a[m, :] + b[m, :]) * gamma + beta over rows of width D
+// (population variance, eps), fp32 statistics; element type `dt` for all.
+cudaError_t launch_add_layernorm(const void* a, const void* b, const void* gamma,
+                                 const void* beta, float eps, void* out, long M, int D,
+                                 mha_dtype dt, cudaStream_t stream);
 
 cudaError_t launch_sdpa_bf16(const SdpaArgs& a, const DeviceCtl& ctl);
 cudaError_t launch_sdpa_f32(const SdpaArgs& a, const DeviceCtl& ctl);

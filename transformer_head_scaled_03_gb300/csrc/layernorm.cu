@@ -1,0 +1,101 @@
+// layernorm.cu -- residual add + LayerNorm, the sublayer wrapper of the
+// post-norm encoder layer: out = LayerNorm(a + b) * gamma + beta per row
+// ("The Transformer" (hoshank.vercel.app), "The Mathematics": output =
+// LayerNorm(x + Sublayer(x)); "The Transformer" (rayaq.ca), "Residuals and
+// LayerNorm": each position rescaled to mean 0 and variance 1, then a
+// learned scale and shift).  Memory-bound: one warp per row, the row held
+// in registers, fp32 statistics with the centred two-pass variance
+// (population variance, divisor D).
+#include <cuda_bf16.h>
+
+#include "internal.h"
+
+namespace mha {
+namespace {
+
+template <typename T>
+__device__ __forceinline__ float to_f(T v);
+template <>
+__device__ __forceinline__ float to_f<float>(float v) { return v; }
+template <>
+__device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
+template <typename T>
+__device__ __forceinline__ T from_f(float v);
+template <>
+__device__ __forceinline__ float from_f<float>(float v) { return v; }
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float v) { return __float2bfloat16_rn(v); }
+
+__device__ __forceinline__ float lane_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+constexpr int kRowsPerBlock = 4;
+
+// VPL: values per lane held in registers (D <= 32 * VPL)
+template <typename T, int VPL>
+__global__ void __launch_bounds__(32 * kRowsPerBlock)
+    add_layernorm_kernel(const T* __restrict__ a, const T* __restrict__ b,
+                         const T* __restrict__ gamma, const T* __restrict__ beta, float eps,
+                         T* __restrict__ out, long M, int D) {
+  const int lane = threadIdx.x & 31;
+  const long row = static_cast<long>(blockIdx.x) * kRowsPerBlock + (threadIdx.x >> 5);
+  if (row >= M) return;  // whole warp leaves together
+  const T* ar = a + row * D;
+  const T* br = b + row * D;
+  float v[VPL];
+  float sum = 0.f;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    const int c = lane + 32 * i;
+    v[i] = c < D ? to_f(ar[c]) + to_f(br[c]) : 0.f;
+    sum += v[i];
+  }
+  const float mean = lane_sum(sum) / static_cast<float>(D);
+  float sq = 0.f;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    const int c = lane + 32 * i;
+    const float dv = c < D ? v[i] - mean : 0.f;
+    sq = fmaf(dv, dv, sq);
+  }
+  const float var = lane_sum(sq) / static_cast<float>(D);
+  const float inv = 1.f / sqrtf(var + eps);
+  T* orow = out + row * D;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    const int c = lane + 32 * i;
+    if (c < D) orow[c] = from_f<T>((v[i] - mean) * inv * to_f(gamma[c]) + to_f(beta[c]));
+  }
+}
+
+template <typename T>
+cudaError_t launch_typed(const void* a, const void* b, const void* g, const void* be, float eps,
+                         void* out, long M, int D, cudaStream_t s) {
+  const dim3 grid(static_cast<unsigned>((M + kRowsPerBlock - 1) / kRowsPerBlock));
+  const dim3 block(32 * kRowsPerBlock);
+  auto args = [&](auto kern) {
+    kern<<<grid, block, 0, s>>>(static_cast<const T*>(a), static_cast<const T*>(b),
+                                static_cast<const T*>(g), static_cast<const T*>(be), eps,
+                                static_cast<T*>(out), M, D);
+  };
+  if (D <= 32 * 16) args(add_layernorm_kernel<T, 16>);
+  else if (D <= 32 * 32) args(add_layernorm_kernel<T, 32>);
+  else if (D <= 32 * 128) args(add_layernorm_kernel<T, 128>);
+  else return cudaErrorInvalidValue;
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_add_layernorm(const void* a, const void* b, const void* gamma,
+                                 const void* beta, float eps, void* out, long M, int D,
+                                 mha_dtype dt, cudaStream_t stream) {
+  if (M == 0) return cudaSuccess;
+  return dt == MHA_BF16 ? launch_typed<__nv_bfloat16>(a, b, gamma, beta, eps, out, M, D, stream)
+                        : launch_typed<float>(a, b, gamma, beta, eps, out, M, D, stream);
+}
+
+}  // namespace mha
