@@ -27,6 +27,7 @@ _LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
 MASK_NONE = 0
 MASK_CAUSAL = 1
 MASK_KEY_PADDING = 2
+MASK_CAUSAL_BOTTOM_RIGHT = 4
 
 _lock = threading.Lock()
 _lib = None

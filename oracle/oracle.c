@@ -20,6 +20,15 @@
  *   triangle, as in the printed 4x4 mask of that section).
  *   Key padding: key j is blocked for every query of batch item b when
  *   j >= key_lengths[b] (one row of the mask per batch item, same section).
+ *   Bottom-right causal (decoding against a cache): the Lq queries are the
+ *   last Lq positions of the len_b tokens whose keys and values are held
+ *   (len_b = key_lengths[b] with key padding, else Lk), so query i sits at
+ *   position len_b - Lq + i and key j is blocked when j > len_b - Lq + i --
+ *   the decoder's restriction to earlier positions applied while generating
+ *   left to right ("How Transformers Work" (worksonmygpu.com), "What changed
+ *   since 2017"; "The Transformer" (hoshank.vercel.app), "The Breakthrough";
+ *   "The Transformer" (rayaq.ca), "The decoder stack").  With Lq == len_b it
+ *   is the causal mask above.
  *   Additive float mask: an optional [Lq, Lk] array A (per batch item and
  *   head through strides, 0 to broadcast) added to the scaled scores like
  *   the causal mask's 0/-inf entries are -- the optional mask of the
@@ -57,11 +66,14 @@
 
 #define ORACLE_MASK_CAUSAL 1
 #define ORACLE_MASK_KEY_PADDING 2
+#define ORACLE_MASK_CAUSAL_BOTTOM_RIGHT 4
 
-/* Additive mask entry M[i][j] for query i, key j (0 or -inf). */
-static double mask_entry(int i, int j, int mask_kind, int len_b)
+/* Additive mask entry M[i][j] for query i of Lq, key j (0 or -inf). */
+static double mask_entry(int i, int j, int mask_kind, int len_b, int Lq)
 {
     if ((mask_kind & ORACLE_MASK_CAUSAL) && j > i)
+        return -INFINITY;
+    if ((mask_kind & ORACLE_MASK_CAUSAL_BOTTOM_RIGHT) && j > len_b - Lq + i)
         return -INFINITY;
     if ((mask_kind & ORACLE_MASK_KEY_PADDING) && j >= len_b)
         return -INFINITY;
@@ -78,7 +90,7 @@ static double mask_entry(int i, int j, int mask_kind, int len_b)
  */
 static int attend_row(const double *q, const double *K, ptrdiff_t ldk,
                       const double *V, ptrdiff_t ldv, int Lk, int d,
-                      double scale, int i, int mask_kind, int len_b,
+                      double scale, int i, int Lq, int mask_kind, int len_b,
                       const double *add_row, double *w, double *o)
 {
     /* scores s_j = scale * <q, k_j> + M_ij (+ A_ij, an additive float mask
@@ -87,7 +99,7 @@ static int attend_row(const double *q, const double *K, ptrdiff_t ldk,
         double dot = 0.0;
         for (int c = 0; c < d; ++c)
             dot += q[c] * K[(ptrdiff_t)j * ldk + c];
-        w[j] = scale * dot + mask_entry(i, j, mask_kind, len_b);
+        w[j] = scale * dot + mask_entry(i, j, mask_kind, len_b, Lq);
         if (add_row)
             w[j] += add_row[j];
     }
@@ -161,7 +173,7 @@ int oracle_sdpa(const double *Q, const double *K, const double *V, double *O,
             const double *arow = add_mask ? add_mask + (int64_t)b * add_stride_b +
                                                 (int64_t)hh * add_stride_h + (int64_t)i * Lk
                                           : NULL;
-            bad += attend_row(Qh + (size_t)i * d, Kh, d, Vh, d, Lk, d, sc, i,
+            bad += attend_row(Qh + (size_t)i * d, Kh, d, Vh, d, Lk, d, sc, i, Lq,
                               mask_kind, len_b, arow, wrow, O + ((size_t)bh * Lq + i) * d);
             if (W)
                 memcpy(W + ((size_t)bh * Lq + i) * Lk, wrow, sizeof(double) * (size_t)Lk);
@@ -202,7 +214,7 @@ int oracle_sdpa_rows(const double *Q, const double *K, const double *V,
                                       : NULL;
         double *wrow = (double *)malloc(sizeof(double) * (size_t)(Lk > 0 ? Lk : 1));
         bad += attend_row(Q + (size_t)rows[r] * d, K + (size_t)bh * Lk * d, d,
-                          V + (size_t)bh * Lk * d, d, Lk, d, sc, i, mask_kind,
+                          V + (size_t)bh * Lk * d, d, Lk, d, sc, i, Lq, mask_kind,
                           len_b, arow, wrow, O_rows + (size_t)r * d);
         free(wrow);
     }
@@ -267,7 +279,7 @@ int oracle_mha(const double *x_q, const double *x_kv, const double *Wq,
             const double *Kh = Kp + (size_t)b * Lk * D + (size_t)hh * d;
             const double *Vh = Vp + (size_t)b * Lk * D + (size_t)hh * d;
             double *o = ctx + ((size_t)b * Lq + i) * D + (size_t)hh * d;
-            bad += attend_row(q, Kh, D, Vh, D, Lk, d, sc, i, mask_kind, len_b, NULL, wrow, o);
+            bad += attend_row(q, Kh, D, Vh, D, Lk, d, sc, i, Lq, mask_kind, len_b, NULL, wrow, o);
         }
         free(wrow);
     }
@@ -382,7 +394,7 @@ int oracle_encoder_layer(const double *x, const double *Wq, const double *Wk,
             const double *Kh = Kp + (size_t)b * L * D + (size_t)hh * d;
             const double *Vh = Vp + (size_t)b * L * D + (size_t)hh * d;
             double *o = ctx + ((size_t)b * L + i) * D + (size_t)hh * d;
-            bad += attend_row(q, Kh, D, Vh, D, L, d, sc, i, mask_kind, len_b, NULL, wrow, o);
+            bad += attend_row(q, Kh, D, Vh, D, L, d, sc, i, L, mask_kind, len_b, NULL, wrow, o);
         }
         free(wrow);
     }

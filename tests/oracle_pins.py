@@ -23,6 +23,12 @@ Sources of the pinned facts:
     multi-head equation.
   - library routines: torch's CPU float64 ``scaled_dot_product_attention``
     and ``multi_head_attention_forward`` (an independent implementation).
+  - decoding: the decoder sees earlier positions only and generates left to
+    right, so attending from the last Lq positions against the cached keys
+    and values reproduces those rows of the full causal pass: "How
+    Transformers Work" (worksonmygpu.com), "What changed since 2017"; "The
+    Transformer" (hoshank.vercel.app), "The Breakthrough"; torch's
+    ``causal_lower_right`` bias is the library cross-check.
 """
 from __future__ import annotations
 
@@ -31,7 +37,7 @@ import os
 
 import numpy as np
 
-from oracle import MASK_CAUSAL, MASK_KEY_PADDING, MASK_NONE
+from oracle import MASK_CAUSAL, MASK_CAUSAL_BOTTOM_RIGHT, MASK_KEY_PADDING, MASK_NONE
 
 GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
 
@@ -509,6 +515,54 @@ def pin_encoder_layernorm_rows(orc):
     perm = rng.permutation(L)
     _allclose(orc.encoder_layer(x[:, perm], p, h), orc.encoder_layer(x, p, h)[:, perm], 1e-11,
               "permutation equivariance")
+
+
+# ------------------------------------------------------- decode-shape pins
+
+def pin_decode_equals_full_causal_rows(orc):
+    """Attending from the last Lq positions of each sequence against a cache
+    of capacity Lmax holding len_b tokens (garbage beyond) reproduces, bit for
+    bit, rows len_b - Lq .. len_b - 1 of the full causal pass; Lq = 1 is key
+    padding alone; Lq = len_b = Lmax is the causal mask."""
+    rng = _rng(40)
+    B, H, n, d, Lmax = 3, 2, 37, 16, 45
+    Qf, Kf, Vf = _qkv(rng, B, H, n, n, d)
+    full = orc.sdpa(Qf, Kf, Vf, mask_kind=MASK_CAUSAL)
+    lens = np.array([37, 20, 5], np.int32)
+    Kc = rng.standard_normal((B, H, Lmax, d)) * 7
+    Vc = rng.standard_normal((B, H, Lmax, d)) * 7
+    for b in range(B):
+        Kc[b, :, : lens[b]] = Kf[b, :, : lens[b]]
+        Vc[b, :, : lens[b]] = Vf[b, :, : lens[b]]
+    mk = MASK_CAUSAL_BOTTOM_RIGHT | MASK_KEY_PADDING
+    for Lq in (1, 4, 5):
+        Q = np.stack([Qf[b, :, lens[b] - Lq: lens[b]] for b in range(B)])
+        O = orc.sdpa(Q, Kc, Vc, mask_kind=mk, key_lengths=lens)
+        assert orc.last_bad_rows == 0
+        for b in range(B):
+            assert np.array_equal(O[b], full[b, :, lens[b] - Lq: lens[b]]), \
+                f"decode rows differ from the causal pass (Lq {Lq}, b {b})"
+        if Lq == 1:
+            Op = orc.sdpa(Q, Kc, Vc, mask_kind=MASK_KEY_PADDING, key_lengths=lens)
+            assert np.array_equal(O, Op), "Lq = 1 is not key padding alone"
+    O = orc.sdpa(Qf, Kf, Vf, mask_kind=MASK_CAUSAL_BOTTOM_RIGHT)
+    assert np.array_equal(O, full), "square bottom-right is not the causal mask"
+
+
+def pin_decode_torch_lower_right(orc):
+    """Library cross-check: torch float64 SDPA with the ``causal_lower_right``
+    bias (Lq <= Lk, no padding)."""
+    import torch
+    import torch.nn.functional as F
+    from torch.nn.attention.bias import causal_lower_right
+    rng = _rng(41)
+    for B, H, Lq, Lk, d in ((2, 3, 1, 50, 16), (1, 2, 7, 19, 8), (2, 1, 16, 200, 32)):
+        Q, K, V = _qkv(rng, B, H, Lq, Lk, d)
+        t = torch.from_numpy
+        ref = F.scaled_dot_product_attention(t(Q), t(K), t(V),
+                                             attn_mask=causal_lower_right(Lq, Lk)).numpy()
+        _allclose(orc.sdpa(Q, K, V, mask_kind=MASK_CAUSAL_BOTTOM_RIGHT), ref, 1e-12,
+                  f"torch lower-right causal {B, H, Lq, Lk, d}")
 
 
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

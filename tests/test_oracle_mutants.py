@@ -29,14 +29,16 @@ MUTANTS = [
     ("mha_scale_uses_dmodel", "const double sc = 1.0 / sqrt((double)d);\n#ifdef",
      "const double sc = 1.0 / sqrt((double)D);\n#ifdef"),
     ("key_proj_uses_wq", "matmul(x_kv, Wk, Kp,", "matmul(x_kv, Wq, Kp,"),
-    ("float_mask_before_scale", "w[j] = scale * dot + mask_entry(i, j, mask_kind, len_b);\n        if (add_row)\n            w[j] += add_row[j];",
-     "w[j] = scale * (dot + (add_row ? add_row[j] : 0.0)) + mask_entry(i, j, mask_kind, len_b);"),
+    ("float_mask_before_scale", "w[j] = scale * dot + mask_entry(i, j, mask_kind, len_b, Lq);\n        if (add_row)\n            w[j] += add_row[j];",
+     "w[j] = scale * (dot + (add_row ? add_row[j] : 0.0)) + mask_entry(i, j, mask_kind, len_b, Lq);"),
     ("float_mask_transposed", "(int64_t)hh * add_stride_h + (int64_t)i * Lk\n                                          : NULL;",
      "(int64_t)hh * add_stride_h + (int64_t)i\n                                          : NULL;"),
     ("layernorm_unbiased_var", "        var /= D;\n", "        var /= (D - 1);\n"),
     ("ffn_no_relu", "hid[i] = hid[i] > 0.0 ? hid[i] : 0.0;", "hid[i] = hid[i];"),
     ("encoder_prenorm_residual", "add_layernorm(x1, f, g2, be2, eps, out, M, D);",
      "add_layernorm(x, f, g2, be2, eps, out, M, D);"),
+    ("decode_top_left_alignment", "j > len_b - Lq + i)", "j > i)"),
+    ("decode_off_by_one", "j > len_b - Lq + i)", "j >= len_b - Lq + i)"),
     ("query_row_stride_wrong", "bad += attend_row(Qh + (size_t)i * d,",
      "bad += attend_row(Qh + (size_t)(Lq - 1 - i) * d,"),
 ]
