@@ -19,6 +19,9 @@ Extra legs in the same JSON line:
                residual + LayerNorm, ReLU FFN d_ff = 4D, residual +
                LayerNorm) in tokens/s, on the key-padding encoder shape
                (B32 L512 D512 h8, bf16) and the base fp32 shape (B1 L128)
+  decode       sdpa_decode (Lq new queries against a bf16 key/value cache,
+               bottom-right causal) on the three decode workloads, in GB/s
+               of cache streamed against the measured HBM peak
   cpu_baseline the fp64 oracle on this host's cores on a bounded row sample
 
 Multi-GPU: the path has no exchange step, so N ranks run N replicas (one per
@@ -113,7 +116,9 @@ def barrier():
 
 
 class ClockSampler:
-    """nvidia-smi clock/throttle samples every 100 ms while active."""
+    """nvidia-smi clock/throttle samples every 20 ms while active.  Entering
+    waits (up to 3 s) for the sampler's first line, so sampling is live when
+    the timed region starts; only lines that arrive after that count."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -124,15 +129,20 @@ class ClockSampler:
         self.proc = None
         self.lines = []
         self._t = None
+        self._start = 0
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self._t = threading.Thread(target=self._read, daemon=True)
             self._t.start()
+            t0 = time.perf_counter()
+            while not self.lines and time.perf_counter() - t0 < 3.0:
+                time.sleep(0.005)
+            self._start = len(self.lines)
         except Exception:
             self.proc = None
         return self
@@ -154,7 +164,7 @@ class ClockSampler:
     def summary(self):
         sms, maxes, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for ln in self.lines[self._start:]:
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 8:
                 continue
@@ -196,6 +206,11 @@ def workload_from_args(args):
     import dataclasses
     from transformer_head_scaled_03_gb300.inputs import WORKLOADS
     w = WORKLOADS[args.workload]
+    if w.kind == "decode":
+        if args.batch is None:
+            return w
+        name = f"{w.name.split(' (')[0]} (B{args.batch} H{w.H} d{w.d}, cache {w.Lk}, reduced)"
+        return dataclasses.replace(w, B=args.batch, name=name)
     if args.seq is None and args.heads is None:
         return w
     L = args.seq if args.seq is not None else w.Lq
@@ -391,6 +406,228 @@ def bench_encoder_layer(shape, dtype_name, steps, warmup, local_rank, key_paddin
             "gpu_launches_per_layer": 7}
 
 
+def bench_decode(w, steps, warmup, local_rank, hbm_peak):
+    """One sdpa_decode over a decode workload: bytes moved per second
+    against the HBM peak (the pass is bound by streaming the cache)."""
+    import torch
+    import transformer_head_scaled_03_gb300 as mha
+    from transformer_head_scaled_03_gb300.inputs import Draws
+
+    dev = torch.device("cuda", local_rank)
+    # the cache is drawn on the device (seeded) to keep the benchmark quick;
+    # the parity tests draw the same shapes through the shared generator
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(w.seed)
+    mk = lambda *shape: torch.randn(*shape, generator=gen, device=dev,
+                                    dtype=torch.float32).to(torch.bfloat16)
+    Q = mk(w.B, w.H, w.Lq, w.d)
+    K = mk(w.B, w.H, w.Lk, w.d)
+    V = mk(w.B, w.H, w.Lk, w.d)
+    lo, hi = w.len_range
+    lens = Draws(w.seed).integers(lo, hi, w.B)
+    kl = torch.from_numpy(lens).to(dev)
+    out = torch.empty_like(Q)
+    splits = mha.decode_splits(w.B, w.H, w.Lk, w.d)
+
+    def step():
+        mha.sdpa_decode(Q, K, V, kv_lengths=kl, causal=True, out=out)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    st = mha.mha_check()
+    if st != mha.MHA_OK:
+        raise RuntimeError(mha.status_string(st))
+    nbytes = w.decode_bytes(lens)
+    gbs = nbytes / (ms / 1e3) / 1e9
+    del K, V
+    return {"workload": w.name, "Lq": w.Lq, "splits": splits,
+            "us_per_call": round(ms * 1e3, 2),
+            "GB_per_s": round(gbs, 1), "hbm_frac": round(gbs / hbm_peak, 4),
+            "bytes_per_call": int(nbytes),
+            "tflops": round(w.flops(lens) / (ms / 1e3) / 1e12, 2),
+            "tokens_per_s": round(w.B * w.Lq / (ms / 1e3), 1),
+            "l2": "cache larger than L2", "gpu_launches_per_call": 1}
+
+
+DECODE_METRIC = "decode attention GB/s of cache streamed (and % of GB300 HBM peak)"
+DECODE_KERNEL_FILES = ["transformer_head_scaled_03_gb300/csrc/sdpa_decode.cu",
+                       "transformer_head_scaled_03_gb300/csrc/ptx.cuh",
+                       "transformer_head_scaled_03_gb300/csrc/ptx_cluster.cuh"]
+
+
+def decode_device_inputs(w, dev):
+    """Seeded device-side draws of one decode workload: Q, the K/V cache, the
+    per-item lengths (host int32 and device)."""
+    import torch
+    from transformer_head_scaled_03_gb300.inputs import Draws
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(w.seed)
+    mk = lambda *shape: torch.randn(*shape, generator=gen, device=dev,
+                                    dtype=torch.float32).to(torch.bfloat16)
+    Q = mk(w.B, w.H, w.Lq, w.d)
+    K = mk(w.B, w.H, w.Lk, w.d)
+    V = mk(w.B, w.H, w.Lk, w.d)
+    lens = Draws(w.seed).integers(w.len_range[0], w.len_range[1], w.B)
+    return Q, K, V, lens, torch.from_numpy(lens).to(dev)
+
+
+def decode_oracle_sample(w, Q, K, V, lens, n_heads, seed):
+    """The oracle as it stands on every query row of ``n_heads`` seeded (b, h)
+    pairs (host float32 copies of those heads); returns GB/s of the cache
+    those rows read, seconds, threads, heads."""
+    import oracle
+    from transformer_head_scaled_03_gb300.inputs import Draws
+    n = min(n_heads, w.B * w.H)
+    bhs = Draws(seed).choice(w.B * w.H, n)
+    host = lambda t, L: (t.reshape(w.B * w.H, L, w.d)[bhs].float().cpu().numpy()[:, None]
+                         if hasattr(t, "cpu") else t.reshape(w.B * w.H, L, w.d)[bhs][:, None])
+    q, k, v = host(Q, w.Lq), host(K, w.Lk), host(V, w.Lk)
+    lb = np.asarray(lens)[bhs // w.H].astype(np.int32)
+    orc = oracle.default()
+    t0 = time.perf_counter()
+    orc.sdpa(q, k, v, mask_kind=w.mask, key_lengths=lb)
+    dt = time.perf_counter() - t0
+    nbytes = 2.0 * w.d * (2.0 * float(np.sum(lb)) + 2.0 * n * w.Lq)
+    return nbytes / dt / 1e9, dt, orc.num_threads(), n
+
+
+def run_gpu_decode(args, w, rank, world, local_rank):
+    """The decode workloads as the benchmark's main step: one sdpa_decode per
+    step over a resident cache; value = whole-job GB/s of cache streamed."""
+    import torch
+    import torch.distributed as dist
+    import transformer_head_scaled_03_gb300 as mha
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    peaks, peak_src = measured_peaks()
+    Q, K, V, lens, kl = decode_device_inputs(w, dev)
+    out = torch.empty_like(Q)
+    nbytes = w.decode_bytes(lens)
+    cache_bytes = 2 * K.numel() * K.element_size()
+    flush = None
+    if cache_bytes < 2 * L2_BYTES:
+        flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+
+    def step():
+        mha.sdpa_decode(Q, K, V, kv_lengths=kl, causal=True, out=out)
+
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert mha.mha_check() == mha.MHA_OK
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clocks:
+        total_ms = 0.0
+        if flush is None:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(args.steps):
+                step()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            total_ms = e0.elapsed_time(e1)
+        else:
+            for _ in range(args.steps):
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                step()
+                e1.record(stream)
+                torch.cuda.synchronize()
+                total_ms += e0.elapsed_time(e1)
+    barrier()
+    torch.cuda.synchronize()
+    st = mha.mha_check()
+    if st != mha.MHA_OK:
+        raise RuntimeError(f"device error during timing: {mha.status_string(st)}")
+    max_s = max_over_ranks(total_ms / 1e3, dev)
+    value = whole_job_value(nbytes * args.steps, world, max_s) / 1e9
+    kernel_gbs = nbytes / (total_ms / 1e3 / args.steps) / 1e9
+
+    # end to end through the public call: the new queries copied in from
+    # pinned host memory and the outputs read back every step (the cache is
+    # the server's resident state)
+    Qh = Q.cpu().pin_memory()
+    Oh = torch.empty_like(Qh).pin_memory()
+    Qd = torch.empty_like(Q)
+    barrier()
+    torch.cuda.synchronize()
+    e2e_steps = max(2, min(args.steps, 20))
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        Qd.copy_(Qh, non_blocking=True)
+        mha.sdpa_decode(Qd, K, V, kv_lengths=kl, causal=True, out=out)
+        Oh.copy_(out, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+        float(Oh[0, 0, 0, 0])
+    e2e_s = max_over_ranks(time.perf_counter() - t0, dev)
+    e2e = {"value": round(whole_job_value(nbytes * e2e_steps, world, e2e_s) / 1e9, 1),
+           "unit": "GB/s", "h2d_bytes_per_step": Qh.numel() * 2,
+           "d2h_bytes_per_step": Oh.numel() * 2,
+           "ms_per_step": round(e2e_s / e2e_steps * 1e3, 4)}
+
+    cpu = None
+    if rank == 0 and not args.skip_cpu:
+        gbs, dt, cores, n = decode_oracle_sample(w, Q, K, V, lens, 64, w.seed + 3000)
+        cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+               "seconds": round(dt, 2),
+               "sample": f"every query row of {n} seeded (b, h) pairs of the same workload, fp64"}
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+    traffic = args.traffic
+    if traffic is None and args.batch is None:
+        traffic = recorded_traffic(DECODE_KERNEL_FILES,
+                                   f"profiles/sdpa_decode_bf16_workload{args.workload}.md")
+    peak = peaks["hbm_gbs"]
+    line = {
+        "metric": DECODE_METRIC,
+        "value": round(value, 1),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(max_s / args.steps * 1e3, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "Lq": w.Lq, "cache": w.Lk, "d": w.d,
+                   "lengths": f"U[{w.len_range[0]}, {w.len_range[1]}]",
+                   "mask": "bottom-right causal + per-item lengths",
+                   "splits": mha.decode_splits(w.B, w.H, w.Lk, w.d),
+                   "bytes_per_step": int(nbytes), "flops_per_step": w.flops(lens),
+                   "l2": "cache larger than L2" if flush is None else "L2 flushed between steps",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "achieved": round(kernel_gbs, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(kernel_gbs / peak, 4),
+                     "peak_source": f"{peak_src} HBM copy", "traffic": traffic,
+                     "kernel": f"sdpa_decode_bf16_kernel<{w.d}>"},
+        "tflops": round(w.flops(lens) / (total_ms / 1e3 / args.steps) / 1e12, 2),
+        "e2e": e2e,
+        "gpu_launches": args.steps,
+        "clocks": clocks.summary(),
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
 def _time_eager_and_graph(step, steps, warmup):
     """(eager ms, CUDA-graph-replay ms) per call of ``step``."""
     import torch
@@ -434,6 +671,9 @@ def run_gpu(args):
         dist.init_process_group(backend="nccl")
     __graft_entry__.build()
     w = workload_from_args(args)
+    if w.kind == "decode":
+        run_gpu_decode(args, w, rank, world, local_rank)
+        return
     r = bench_sdpa(args, w, rank, world, local_rank)
     peaks, peak_src = measured_peaks()
 
@@ -449,6 +689,11 @@ def run_gpu(args):
             bench_encoder_layer((w2.B, w2.Lq, w2.H * w2.d, w2.H, 4 * w2.H * w2.d), "bf16", 20, 3,
                                 local_rank, key_padding=w2.len_range),
             bench_encoder_layer((1, 128, 512, 8, 2048), "f32", 100, 5, local_rank)]
+
+    decode = None
+    if not args.skip_decode:
+        decode = [bench_decode(WORKLOADS[i], 50, 5, local_rank, peaks["hbm_gbs"])
+                  for i in (6, 7, 8)]
 
     cpu = None
     if rank == 0 and not args.skip_cpu:
@@ -501,6 +746,7 @@ def run_gpu(args):
         "cpu_baseline": cpu,
         "mha_layer": mha_layer,
         "encoder_layer": encoder_layer,
+        "decode": decode,
     }
     print(json.dumps(line), flush=True)
     if world > 1:
@@ -517,6 +763,9 @@ def run_reference(args):
     from transformer_head_scaled_03_gb300.inputs import WORKLOADS, sample_rows, sdpa_inputs
 
     w = workload_from_args(args)
+    if w.kind == "decode":
+        run_reference_decode(args, w, world)
+        return
     Q, K, V, lens, _ = sdpa_inputs(w)
     rows = sample_rows(w.B, w.H, w.Lq, args.ref_rows_per_head, seed=w.seed + 4000, must=())
     for _ in range(args.warmup):
@@ -544,13 +793,56 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_reference_decode(args, w, world):
+    """The oracle on a seeded sample of (b, h) pairs of a decode workload,
+    drawn on the host with the shared generator (only the sampled heads)."""
+    from transformer_head_scaled_03_gb300.inputs import Draws
+    n = min(16, w.B * w.H)
+    g = Draws(w.seed + 5000)
+    Q = g.normal((w.B * w.H, w.Lq, w.d))
+    lens = Draws(w.seed).integers(w.len_range[0], w.len_range[1], w.B)
+    # only the sampled heads' cache rows are drawn; the rest is never read
+    bhs = Draws(w.seed + 4000).choice(w.B * w.H, n)
+    Ks = g.normal((n, w.Lk, w.d))
+    Vs = g.normal((n, w.Lk, w.d))
+    lb = lens[bhs // w.H].astype(np.int32)
+    import oracle
+    orc = oracle.default()
+    total_s, total_bytes = 0.0, 0.0
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        orc.sdpa(Q[bhs][:, None], Ks[:, None], Vs[:, None], mask_kind=w.mask, key_lengths=lb)
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            total_s += dt
+            total_bytes += 2.0 * w.d * (2.0 * float(np.sum(lb)) + 2.0 * n * w.Lq)
+    value = total_bytes / total_s / 1e9
+    sample = (f"every query row of {n} seeded (b, h) pairs per step, their cache rows "
+              f"drawn on the host, fp64 oracle")
+    line = {
+        "impl": "reference", "metric": DECODE_METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(total_s / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "Lq": w.Lq, "cache": w.Lk, "d": w.d},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": orc.num_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=60)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
-    ap.add_argument("--workload", type=int, default=5, choices=[2, 3, 4, 5])
+    ap.add_argument("--workload", type=int, default=5, choices=[2, 3, 4, 5, 6, 7, 8],
+                    help="2-5: attention workloads; 6-8: decode against a cache")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override the batch size of a decode workload (profiling captures)")
     ap.add_argument("--seq", type=int, default=None,
                     help="override the sequence length (profiling captures)")
     ap.add_argument("--heads", type=int, default=None,
@@ -559,6 +851,7 @@ def main(argv=None):
                     help="pass the causal mask as an additive float mask [Lq, Lk]")
     ap.add_argument("--skip-mha", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--skip-decode", action="store_true")
     ap.add_argument("--cpu-rows-per-head", type=int, default=None,
                     help="oracle CPU-baseline sample (default: about 10 s of work)")
     ap.add_argument("--ref-rows-per-head", type=int, default=4)

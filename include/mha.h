@@ -60,8 +60,13 @@ typedef enum { MHA_F32 = 0, MHA_BF16 = 1 } mha_dtype;
 enum {
     MHA_MASK_NONE = 0,
     MHA_MASK_CAUSAL = 1,
-    MHA_MASK_KEY_PADDING = 2
+    MHA_MASK_KEY_PADDING = 2,
+    /* sdpa_decode only: query i of Lq sees keys j <= len_b - Lq + i */
+    MHA_MASK_CAUSAL_BOTTOM_RIGHT = 4
 };
+
+/* Largest number of new queries per (batch item, head) sdpa_decode takes. */
+#define MHA_DECODE_MAX_QUERIES 16
 
 /* Same type as cudaStream_t, declared here so the header needs no CUDA
  * include. */
@@ -114,6 +119,45 @@ mha_status sdpa_forward_float_mask(const void *Q, const void *K, const void *V,
                                    int64_t mask_stride_b,
                                    int64_t mask_stride_h, mha_dtype in_dtype,
                                    mha_dtype out_dtype, mha_stream stream);
+
+/*
+ * sdpa_decode -- attention of Lq <= 16 new queries per (batch item, head)
+ * against a key/value cache: the decoder's masked self-attention while it
+ * generates left to right, reusing the keys and values it has stored ("How
+ * Transformers Work" (worksonmygpu.com), "What changed since 2017"; "The
+ * Transformer" (hoshank.vercel.app), "The Breakthrough"; "The Transformer"
+ * (rayaq.ca), "The decoder stack").
+ *   Q       [B, H, Lq, d] bf16: the queries of the newest Lq positions.
+ *   K_cache [B, H, Lk, d] bf16, V_cache [B, H, Lk, d] bf16: a cache of
+ *           capacity Lk; batch item b holds len_b tokens in rows
+ *           [0, len_b), the newest Lq of them being the queries' own.
+ *   O       [B, H, Lq, d], out_dtype BF16 or F32.
+ *   scale   : as for sdpa_forward (0 selects 1/sqrt(d)).
+ *   mask_kind : bit set of MHA_MASK_KEY_PADDING (len_b = kv_lengths[b]; else
+ *           every item holds Lk tokens) and MHA_MASK_CAUSAL_BOTTOM_RIGHT
+ *           (query i sees keys j <= len_b - Lq + i; without it every query
+ *           sees all len_b keys, as cross-attention to an encoder memory).
+ *           MHA_MASK_CAUSAL is not accepted here.
+ *   kv_lengths : device int32[B], given iff KEY_PADDING is set; each value
+ *           must lie in [1, Lk], and in [Lq, Lk] with the causal bit
+ *           (checked on the device: MHA_ERR_DEVICE from mha_check, rows
+ *           written as zeros).
+ *   num_splits : CTAs that share one (b, h)'s keys, 1..16, merged exactly
+ *           through one thread-block cluster; 0 picks a default
+ *           (sdpa_decode_splits).
+ * d must be 64 or 128; Q, K_cache, V_cache and O 16-byte aligned.  B or H
+ * may be 0 (nothing is launched).  The call allocates nothing.
+ * Returns MHA_OK, MHA_ERR_INVALID_ARG, MHA_ERR_UNSUPPORTED (Lq > 16, other
+ * d) or MHA_ERR_CUDA.
+ */
+mha_status sdpa_decode(const void *Q, const void *K_cache, const void *V_cache,
+                       void *O, int B, int H, int Lq, int Lk, int d,
+                       float scale, int mask_kind, const int32_t *kv_lengths,
+                       mha_dtype out_dtype, int num_splits,
+                       mha_stream stream);
+
+/* The split count sdpa_decode uses for num_splits = 0 (0 for bad sizes). */
+int sdpa_decode_splits(int B, int H, int Lk, int d);
 
 /*
  * mha_create -- allocate a multi-head attention layer handle.

@@ -29,6 +29,7 @@ MHA_BF16 = 1
 MASK_NONE = 0
 MASK_CAUSAL = 1
 MASK_KEY_PADDING = 2
+MASK_CAUSAL_BOTTOM_RIGHT = 4
 
 LIB_PATH = _build.LIB
 
@@ -56,6 +57,11 @@ def _declare(lib):
     lib.sdpa_forward.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, i32, vp,
                                  i32, i32, vp]
     lib.sdpa_forward.restype = i32
+    lib.sdpa_decode.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, i32, vp, i32, i32,
+                                vp]
+    lib.sdpa_decode.restype = i32
+    lib.sdpa_decode_splits.argtypes = [i32, i32, i32, i32]
+    lib.sdpa_decode_splits.restype = i32
     i64 = ctypes.c_int64
     lib.sdpa_forward_float_mask.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, i32,
                                             vp, vp, i64, i64, i32, i32, vp]
@@ -181,6 +187,40 @@ def sdpa_forward(Q, K, V, scale: float | None = None, mask_kind: int = MASK_NONE
                             _dtype_code(Q.dtype), _dtype_code(odt), _stream(stream))
     _check(st, "sdpa_forward")
     return out
+
+
+def sdpa_decode(Q, K_cache, V_cache, kv_lengths=None, causal: bool = True,
+                scale: float | None = None, out_dtype: torch.dtype | None = None,
+                num_splits: int = 0, out=None, stream=None):
+    """Decode-shape attention: Q [B,H,Lq<=16,d] (the newest Lq positions)
+    against caches K/V [B,H,Lk,d] holding kv_lengths[b] tokens (all Lk when
+    None); bottom-right causal unless ``causal`` is False."""
+    B, H, Lq, d = Q.shape
+    Lk = K_cache.shape[2]
+    if K_cache.shape != (B, H, Lk, d) or V_cache.shape != (B, H, Lk, d):
+        raise ValueError("Q/cache shapes disagree")
+    if K_cache.dtype != Q.dtype or V_cache.dtype != Q.dtype:
+        raise ValueError("Q/cache dtypes disagree")
+    odt = out_dtype or Q.dtype
+    if out is None:
+        out = torch.empty((B, H, Lq, d), dtype=odt, device=Q.device)
+    elif out.shape != (B, H, Lq, d) or out.dtype != odt:
+        raise ValueError("out has the wrong shape or dtype")
+    mask = MASK_CAUSAL_BOTTOM_RIGHT if causal else MASK_NONE
+    if kv_lengths is not None:
+        if kv_lengths.dtype != torch.int32:
+            raise ValueError("kv_lengths must be int32")
+        mask |= MASK_KEY_PADDING
+    st = lib().sdpa_decode(_dev_ptr(Q), _dev_ptr(K_cache), _dev_ptr(V_cache), _dev_ptr(out), B, H,
+                           Lq, Lk, d, float(scale or 0.0), mask, _dev_ptr(kv_lengths),
+                           _dtype_code(odt), int(num_splits), _stream(stream))
+    _check(st, "sdpa_decode")
+    return out
+
+
+def decode_splits(B: int, H: int, Lk: int, d: int) -> int:
+    """The split count sdpa_decode picks by default."""
+    return int(lib().sdpa_decode_splits(B, H, Lk, d))
 
 
 class MhaHandle:

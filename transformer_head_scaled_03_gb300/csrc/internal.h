@@ -64,6 +64,24 @@ cudaError_t launch_add_layernorm(const void* a, const void* b, const void* gamma
                                  const void* beta, float eps, void* out, long M, int D,
                                  mha_dtype dt, cudaStream_t stream);
 
+// One decode-shape attention launch (bf16 cache).
+struct DecodeArgs {
+  const void* Q;  // [B, H, Lq, d]
+  const void* K;  // [B, H, Lk, d] cache
+  const void* V;
+  void* O;        // [B, H, Lq, d]
+  int B, H, Lq, Lk, d;
+  float scale;    // resolved (> 0)
+  bool causal;    // bottom-right
+  const int32_t* kv_len;  // device [B] or nullptr
+  mha_dtype out_dtype;
+  int splits;
+  cudaStream_t stream;
+};
+
+cudaError_t launch_sdpa_decode_bf16(const DecodeArgs& a, const DeviceCtl& ctl);
+int decode_default_splits(int B, int H, int Lk, int d);
+
 cudaError_t launch_sdpa_bf16(const SdpaArgs& a, const DeviceCtl& ctl);
 cudaError_t launch_sdpa_f32(const SdpaArgs& a, const DeviceCtl& ctl);
 cudaError_t launch_gemm_bf16(const GemmArgs& g, const DeviceCtl& ctl);

@@ -26,6 +26,7 @@ import numpy as np
 MASK_NONE = 0
 MASK_CAUSAL = 1
 MASK_KEY_PADDING = 2
+MASK_CAUSAL_BOTTOM_RIGHT = 4
 
 SEED_BASE = 0x5EED0000
 
@@ -92,10 +93,22 @@ class Workload:
         B, H, Lq, Lk, d = self.B, self.H, self.Lq, self.Lk, self.d
         if self.mask & MASK_CAUSAL:
             return 2.0 * B * H * d * Lq * (Lq + 1)
+        if self.mask & MASK_CAUSAL_BOTTOM_RIGHT:
+            # query i of Lq sees len_b - Lq + i + 1 keys
+            lens = (np.full(B, Lk) if key_lengths is None
+                    else np.asarray(key_lengths, dtype=np.float64))
+            pairs = float(np.sum(Lq * (lens - Lq) + Lq * (Lq + 1) / 2.0))
+            return 4.0 * H * d * pairs
         if self.mask & MASK_KEY_PADDING:
             assert key_lengths is not None
             return 4.0 * H * Lq * d * float(np.sum(key_lengths))
         return 4.0 * B * H * Lq * Lk * d
+
+    def decode_bytes(self, key_lengths=None) -> float:
+        """Algorithmic HBM bytes of one decode pass (bf16): every held key and
+        value row read once, the queries read and the outputs written once."""
+        lens = np.full(self.B, self.Lk) if key_lengths is None else np.asarray(key_lengths)
+        return 2.0 * self.H * self.d * (2.0 * float(np.sum(lens)) + 2.0 * self.B * self.Lq)
 
 
 WORKLOADS = {
@@ -111,6 +124,17 @@ WORKLOADS = {
     5: Workload(5, "long-context causal (B1 L32768 H32 d128 bf16, outlier dims)", "sdpa",
                 "bf16", B=1, H=32, Lq=32768, Lk=32768, d=128, mask=MASK_CAUSAL,
                 outliers=(4, 8.0)),
+    # decoding against a cache: the newest Lq positions of each sequence attend
+    # to its len_b cached keys (bottom-right causal); lengths vary per item
+    6: Workload(6, "decode, one new token (B8 H32 d128, cache 32768, lengths U[16384, 32768] bf16)",
+                "decode", "bf16", B=8, H=32, Lq=1, Lk=32768, d=128,
+                mask=MASK_CAUSAL_BOTTOM_RIGHT | MASK_KEY_PADDING, len_range=(16384, 32768)),
+    7: Workload(7, "decode, 16 new tokens (B8 H32 d128, cache 32768, lengths U[16384, 32768] bf16)",
+                "decode", "bf16", B=8, H=32, Lq=16, Lk=32768, d=128,
+                mask=MASK_CAUSAL_BOTTOM_RIGHT | MASK_KEY_PADDING, len_range=(16384, 32768)),
+    8: Workload(8, "decode, base width (B64 H8 d64, cache 4096, lengths U[1024, 4096] bf16)",
+                "decode", "bf16", B=64, H=8, Lq=1, Lk=4096, d=64,
+                mask=MASK_CAUSAL_BOTTOM_RIGHT | MASK_KEY_PADDING, len_range=(1024, 4096)),
 }
 
 
