@@ -67,6 +67,10 @@ def _declare(lib):
     lib.oracle_encoder_layer.restype = c_int
     lib.oracle_encoder_layer_num_params.argtypes = [c_int, c_int]
     lib.oracle_encoder_layer_num_params.restype = ctypes.c_long
+    lib.oracle_sinusoidal_pe.argtypes = [dp, c_int, c_int, c_int]
+    lib.oracle_sinusoidal_pe.restype = None
+    lib.oracle_embed_pe.argtypes = [ip, dp, c_int, dp, c_int, c_int, c_int, c_int, c_double]
+    lib.oracle_embed_pe.restype = c_int
     lib.oracle_num_threads.argtypes = []
     lib.oracle_num_threads.restype = c_int
     return lib
@@ -220,6 +224,29 @@ def _encoder_num_params(self, D: int, F: int) -> int:
     return int(self.lib.oracle_encoder_layer_num_params(D, F))
 
 
+def _sinusoidal_pe(self, n_pos: int, D: int, first_pos: int = 0):
+    """PE rows first_pos .. first_pos + n_pos - 1 -> [n_pos, D]."""
+    pe = np.empty((n_pos, D))
+    self.lib.oracle_sinusoidal_pe(_ptr(pe), int(first_pos), int(n_pos), int(D))
+    return pe
+
+
+def _embed_pe(self, ids, table, pos_offset: int = 0, scale: float = 0.0):
+    """ids [B, L] int32, table [vocab, D] -> x [B, L, D] = table[ids] * scale
+    + PE(pos_offset + l) (scale 0 selects sqrt(D))."""
+    ids = np.ascontiguousarray(np.asarray(ids, dtype=np.int32))
+    table = _d(table)
+    B, L = ids.shape
+    vocab, D = table.shape
+    x = np.empty((B, L, D))
+    bad = self.lib.oracle_embed_pe(_ptr(ids, ctypes.c_int32), _ptr(table), vocab, _ptr(x), B, L,
+                                   D, int(pos_offset), float(scale))
+    self.last_bad_rows = int(bad)
+    return x
+
+
+Oracle.sinusoidal_pe = _sinusoidal_pe
+Oracle.embed_pe = _embed_pe
 Oracle.encoder_layer = _encoder_layer
 Oracle.encoder_num_params = _encoder_num_params
 
@@ -247,3 +274,11 @@ def mha(*a, **k):
 
 def encoder_layer(*a, **k):
     return default().encoder_layer(*a, **k)
+
+
+def sinusoidal_pe(*a, **k):
+    return default().sinusoidal_pe(*a, **k)
+
+
+def embed_pe(*a, **k):
+    return default().embed_pe(*a, **k)

@@ -427,6 +427,61 @@ long oracle_encoder_layer_num_params(int D, int F)
            + 2L * (D + D);              /* two LayerNorms: gamma, beta */
 }
 
+/*
+ * Sinusoidal positional encoding, [n_pos, D] row-major:
+ *   PE(pos, 2i)   = sin(pos / 10000^(2i / D))
+ *   PE(pos, 2i+1) = cos(pos / 10000^(2i / D))
+ * for positions first_pos .. first_pos + n_pos - 1 -- "How Transformers
+ * Work" (worksonmygpu.com), "Positional encoding"; "The Transformer"
+ * (hoshank.vercel.app), "The Mathematics", the last pair of equations (pos
+ * counts from 0; i indexes the dimension pair).  An odd D leaves the last
+ * column a sine.
+ */
+void oracle_sinusoidal_pe(double *pe, int first_pos, int n_pos, int D)
+{
+    for (int r = 0; r < n_pos; ++r) {
+        const double pos = (double)(first_pos + r);
+        for (int c = 0; c < D; ++c) {
+            const int i = c / 2;
+            const double angle = pos / pow(10000.0, (2.0 * i) / (double)D);
+            pe[(size_t)r * D + c] = (c % 2 == 0) ? sin(angle) : cos(angle);
+        }
+    }
+}
+
+/*
+ * Input of the first layer: x[b, l, :] = table[ids[b, l], :] * scale
+ * + PE(pos_offset + l, :), the token embedding scaled by sqrt(d_model) plus
+ * the positional encoding ("The Transformer" (rayaq.ca), "Embeddings and
+ * positions" and the encode() step of "Implementation"; "The Transformer"
+ * (hoshank.vercel.app): the encodings are added to the input embeddings).
+ * scale == 0 selects sqrt(D).  Returns the number of ids outside
+ * [0, vocab); their rows are NaN.
+ */
+int oracle_embed_pe(const int32_t *ids, const double *table, int vocab, double *x, int B,
+                    int L, int D, int pos_offset, double scale)
+{
+    const double sc = scale == 0.0 ? sqrt((double)D) : scale;
+    double *pe = (double *)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1) * (size_t)D);
+    oracle_sinusoidal_pe(pe, pos_offset, L, D);
+    int bad = 0;
+    for (int b = 0; b < B; ++b)
+        for (int l = 0; l < L; ++l) {
+            const int32_t id = ids[(size_t)b * L + l];
+            double *row = x + ((size_t)b * L + l) * D;
+            if (id < 0 || id >= vocab) {
+                for (int c = 0; c < D; ++c)
+                    row[c] = NAN;
+                ++bad;
+                continue;
+            }
+            for (int c = 0; c < D; ++c)
+                row[c] = table[(size_t)id * D + c] * sc + pe[(size_t)l * D + c];
+        }
+    free(pe);
+    return bad;
+}
+
 int oracle_num_threads(void)
 {
 #ifdef _OPENMP

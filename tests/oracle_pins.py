@@ -23,6 +23,13 @@ Sources of the pinned facts:
     multi-head equation.
   - library routines: torch's CPU float64 ``scaled_dot_product_attention``
     and ``multi_head_attention_forward`` (an independent implementation).
+  - positional encoding: PE(0, 2i) = 0 and PE(0, 2i+1) = 1; each dimension
+    pair is a point on the unit circle turning at its own frequency, the
+    frequencies falling geometrically from 1 rad per position, so a shift of
+    k positions is one fixed rotation per pair (the "signal for relative
+    position"): "How Transformers Work" (worksonmygpu.com), "Positional
+    encoding"; "The Transformer" (hoshank.vercel.app), "The Mathematics".
+    The embedding lookup is cross-checked against torch's embedding.
   - decoding: the decoder sees earlier positions only and generates left to
     right, so attending from the last Lq positions against the cached keys
     and values reproduces those rows of the full causal pass: "How
@@ -563,6 +570,62 @@ def pin_decode_torch_lower_right(orc):
                                              attn_mask=causal_lower_right(Lq, Lk)).numpy()
         _allclose(orc.sdpa(Q, K, V, mask_kind=MASK_CAUSAL_BOTTOM_RIGHT), ref, 1e-12,
                   f"torch lower-right causal {B, H, Lq, Lk, d}")
+
+
+# ------------------------------------------------------ positional encoding
+
+def pin_pe_position_zero(orc):
+    """At position 0 every sine column is 0 and every cosine column is 1."""
+    for D in (8, 64, 512, 7):
+        pe = orc.sinusoidal_pe(1, D)[0]
+        assert np.all(pe[0::2] == 0.0) and np.all(pe[1::2] == 1.0), D
+
+
+def pin_pe_pairs_rotate(orc):
+    """Each (sin, cos) pair lies on the unit circle, and shifting the position
+    by k turns every pair by the angle it has at position k: a fixed
+    rotation per pair, whatever the start position."""
+    D = 64
+    pe = orc.sinusoidal_pe(300, D)
+    s, c = pe[:, 0::2], pe[:, 1::2]
+    _allclose(s * s + c * c, np.ones_like(s), 1e-14, "unit circle")
+    for k in (1, 7, 100):
+        sk, ck = s[k], c[k]          # position k from position 0 = (0, 1)
+        pred_s = s[:-k] * ck + c[:-k] * sk
+        pred_c = c[:-k] * ck - s[:-k] * sk
+        _allclose(pred_s, s[k:], 1e-11, f"shift {k} (sin)")
+        _allclose(pred_c, c[k:], 1e-11, f"shift {k} (cos)")
+
+
+def pin_pe_frequencies(orc):
+    """Pair 0 turns 1 rad per position; each next pair turns slower by the
+    same factor, down to 1/10000 rad per position (10000^(-2/D) per pair)."""
+    for D in (16, 512):
+        pe = orc.sinusoidal_pe(2, D)
+        w = np.arctan2(pe[1, 0::2], pe[1, 1::2])   # angle turned in one position
+        assert abs(w[0] - 1.0) < 1e-15
+        ratios = w[1:] / w[:-1]
+        _allclose(ratios, np.full_like(ratios, 10000.0 ** (-2.0 / D)), 1e-12, f"ratio D={D}")
+        assert abs(math.log(w[-1] / w[0]) / math.log(1e-4) - (D - 2) / D) < 1e-12
+
+
+def pin_embed_torch_and_offset(orc):
+    """x = embedding * sqrt(D) + PE: the lookup against torch's embedding in
+    float64, and a window starting at position k equals columns k.. of the
+    whole sequence (the position offset)."""
+    import torch
+    rng = _rng(50)
+    vocab, D, B, L = 37, 16, 2, 9
+    table = rng.standard_normal((vocab, D))
+    ids = rng.integers(0, vocab, size=(B, L)).astype(np.int32)
+    x = orc.embed_pe(ids, table)
+    emb = torch.nn.functional.embedding(torch.from_numpy(ids.astype(np.int64)),
+                                        torch.from_numpy(table)).numpy()
+    _allclose(x - orc.sinusoidal_pe(L, D)[None], emb * math.sqrt(D), 1e-12, "torch embedding")
+    for k in (1, 4):
+        assert np.array_equal(orc.embed_pe(ids[:, k:].copy(), table, pos_offset=k), x[:, k:])
+    _allclose(orc.embed_pe(ids, table, scale=1.0) - orc.sinusoidal_pe(L, D)[None], emb, 1e-12,
+              "explicit scale 1")
 
 
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

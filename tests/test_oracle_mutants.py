@@ -39,6 +39,13 @@ MUTANTS = [
      "add_layernorm(x, f, g2, be2, eps, out, M, D);"),
     ("decode_top_left_alignment", "j > len_b - Lq + i)", "j > i)"),
     ("decode_off_by_one", "j > len_b - Lq + i)", "j >= len_b - Lq + i)"),
+    ("pe_sin_cos_swapped", "(c % 2 == 0) ? sin(angle) : cos(angle)",
+     "(c % 2 == 0) ? cos(angle) : sin(angle)"),
+    ("pe_exponent_i_over_d", "(2.0 * i) / (double)D", "(double)i / (double)D"),
+    ("pe_pair_index_is_column", "const int i = c / 2;", "const int i = c;"),
+    ("pe_offset_ignored", "const double pos = (double)(first_pos + r);",
+     "const double pos = (double)(r);"),
+    ("embed_not_scaled", "scale == 0.0 ? sqrt((double)D) : scale", "scale == 0.0 ? 1.0 : scale"),
     ("query_row_stride_wrong", "bad += attend_row(Qh + (size_t)i * d,",
      "bad += attend_row(Qh + (size_t)(Lq - 1 - i) * d,"),
 ]
