@@ -19,6 +19,10 @@ Extra legs in the same JSON line:
                residual + LayerNorm, ReLU FFN d_ff = 4D, residual +
                LayerNorm) in tokens/s, on the key-padding encoder shape
                (B32 L512 D512 h8, bf16) and the base fp32 shape (B1 L128)
+  embed_pe     the first layer's input (embedding x sqrt(D) + positional
+               encoding, one pass) in GB/s on the encoder shape with the
+               pages' 37000-token vocabulary, and tokens/s of that pass plus
+               one encoder layer
   decode       sdpa_decode (Lq new queries against a bf16 key/value cache,
                bottom-right causal) on the three decode workloads, in GB/s
                of cache streamed against the measured HBM peak
@@ -628,6 +632,62 @@ def run_gpu_decode(args, w, rank, world, local_rank):
         dist.destroy_process_group()
 
 
+def bench_embed_pe(shape, steps, warmup, local_rank, hbm_peak, layer_shape=None):
+    """embed_pe_forward (embedding x sqrt(D) + PE, one pass) in GB/s against
+    the HBM peak; with ``layer_shape`` (h, d_ff) also the embedding pass plus
+    one encoder layer, tokens/s (CUDA graph replay of both calls)."""
+    import torch
+    import transformer_head_scaled_03_gb300 as mha
+    from transformer_head_scaled_03_gb300.inputs import Draws
+
+    B, L, D, vocab = shape
+    dev = torch.device("cuda", local_rank)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(0x5EED0300 + D)
+    table = (torch.randn(vocab, D, generator=gen, device=dev) / math.sqrt(D)).to(torch.bfloat16)
+    ids = torch.from_numpy(Draws(0x5EED0300 + L).integers(0, vocab - 1, (B, L))).to(dev)
+    pe = mha.sinusoidal_pe(L, D, device=dev)
+    x = torch.empty((B, L, D), dtype=torch.bfloat16, device=dev)
+    eager_ms, graph_ms = _time_eager_and_graph(lambda: mha.embed_pe(ids, table, pe, out=x),
+                                               steps, warmup)
+    rows = B * L
+    nbytes = rows * (2 * D + 2 * D + 4) + L * D * 4
+    out = {"shape": {"B": B, "L": L, "D": D, "vocab": vocab, "dtype": "bf16"},
+           "us_per_call": round(graph_ms * 1e3, 2), "GB_per_s": round(nbytes / graph_ms / 1e6, 1),
+           "hbm_frac": round(nbytes / graph_ms / 1e6 / hbm_peak, 4),
+           "bytes_per_call": nbytes, "tokens_per_s": round(rows / (graph_ms / 1e3), 1),
+           "timing": "CUDA graph replay", "gpu_launches_per_call": 1}
+    if layer_shape is not None:
+        h, F = layer_shape
+        g = Draws(0x5EED0400 + D)
+        mk = lambda a: torch.from_numpy(a).to(torch.bfloat16).to(dev)
+        p = {n: mk(g.normal((D, D), std=1.0 / math.sqrt(D), dtype="bf16"))
+             for n in ("Wq", "Wk", "Wv", "Wo")}
+        p["W1"] = mk(g.normal((D, F), std=1.0 / math.sqrt(D), dtype="bf16"))
+        p["W2"] = mk(g.normal((F, D), std=1.0 / math.sqrt(F), dtype="bf16"))
+        for n in ("bq", "bk", "bv", "bo", "b2", "ln1_beta", "ln2_beta"):
+            p[n] = mk(g.normal((D,), std=0.1, dtype="bf16"))
+        p["b1"] = mk(g.normal((F,), std=0.1, dtype="bf16"))
+        for n in ("ln1_gamma", "ln2_gamma"):
+            p[n] = mk(1.0 + g.normal((D,), std=0.1, dtype="f32"))
+        y = torch.empty_like(x)
+        layer = mha.EncoderLayer(D, h, F, torch.bfloat16, B, L)
+        try:
+            def both():
+                mha.embed_pe(ids, table, pe, out=x)
+                layer.forward(x, p, out=y)
+            _, both_ms = _time_eager_and_graph(both, steps, warmup)
+        finally:
+            layer.close()
+        out["with_encoder_layer"] = {"h": h, "d_ff": F, "ms": round(both_ms, 4),
+                                     "tokens_per_s": round(rows / (both_ms / 1e3), 1),
+                                     "gpu_launches": 8}
+    st = mha.mha_check()
+    if st != mha.MHA_OK:
+        raise RuntimeError(mha.status_string(st))
+    return out
+
+
 def _time_eager_and_graph(step, steps, warmup):
     """(eager ms, CUDA-graph-replay ms) per call of ``step``."""
     import torch
@@ -683,12 +743,16 @@ def run_gpu(args):
                      bench_mha_layer((1, 128, 512, 8), "f32", 200, 5, local_rank,
                                      seed_w=WORKLOADS[1].seed)]
     encoder_layer = None
+    embed = None
     if not args.skip_mha:
         w2 = WORKLOADS[2]
         encoder_layer = [
             bench_encoder_layer((w2.B, w2.Lq, w2.H * w2.d, w2.H, 4 * w2.H * w2.d), "bf16", 20, 3,
                                 local_rank, key_padding=w2.len_range),
             bench_encoder_layer((1, 128, 512, 8, 2048), "f32", 100, 5, local_rank)]
+        w2 = WORKLOADS[2]
+        embed = bench_embed_pe((w2.B, w2.Lq, w2.H * w2.d, 37000), 20, 3, local_rank,
+                               peaks["hbm_gbs"], layer_shape=(w2.H, 4 * w2.H * w2.d))
 
     decode = None
     if not args.skip_decode:
@@ -746,6 +810,7 @@ def run_gpu(args):
         "cpu_baseline": cpu,
         "mha_layer": mha_layer,
         "encoder_layer": encoder_layer,
+        "embed_pe": embed,
         "decode": decode,
     }
     print(json.dumps(line), flush=True)

@@ -160,6 +160,40 @@ mha_status sdpa_decode(const void *Q, const void *K_cache, const void *V_cache,
 int sdpa_decode_splits(int B, int H, int Lk, int d);
 
 /*
+ * sinusoidal_pe -- the positional-encoding table, fp32 [n_pos, d_model]:
+ * row r holds PE(first_pos + r, :) with PE(pos, 2i) = sin(pos / 10000^(2i/D))
+ * and PE(pos, 2i+1) = cos(pos / 10000^(2i/D)) ("How Transformers Work"
+ * (worksonmygpu.com), "Positional encoding"; "The Transformer"
+ * (hoshank.vercel.app), "The Mathematics").  Each value is the fp64 sine or
+ * cosine of the fp64 angle, rounded to fp32.  pe: device, 4-byte aligned,
+ * caller-owned.  Built once per length and reused.
+ * Returns MHA_OK, MHA_ERR_INVALID_ARG or MHA_ERR_CUDA.
+ */
+mha_status sinusoidal_pe(float *pe, int first_pos, int n_pos, int d_model,
+                         mha_stream stream);
+
+/*
+ * embed_pe_forward -- the first layer's input in one pass:
+ *   x[b, l, :] = table[ids[b, l], :] * scale + pe[pos_offset + l, :]
+ * the token embedding scaled by sqrt(d_model) plus the positional encoding
+ * ("The Transformer" (rayaq.ca), "Embeddings and positions" and the encode
+ * step of "Implementation").
+ *   ids   : device int32 [B, L]; each must lie in [0, vocab) (checked on the
+ *           device: MHA_ERR_DEVICE from mha_check, the row written as zeros).
+ *   table : device [vocab, d_model] of dtype (BF16 or F32), 16-byte aligned.
+ *   pe    : device fp32 [pe_rows, d_model] from sinusoidal_pe (first_pos 0),
+ *           16-byte aligned; pos_offset + L <= pe_rows.
+ *   x     : device [B, L, d_model] of dtype, 16-byte aligned; the sum is
+ *           taken in fp32 and rounded once.
+ *   scale : 0 selects sqrt(d_model); otherwise finite and >= 0.
+ * Returns MHA_OK, MHA_ERR_INVALID_ARG or MHA_ERR_CUDA.
+ */
+mha_status embed_pe_forward(const int32_t *ids, const void *table, int vocab,
+                            const float *pe, int pe_rows, void *x, int B,
+                            int L, int d_model, int pos_offset, float scale,
+                            mha_dtype dtype, mha_stream stream);
+
+/*
  * mha_create -- allocate a multi-head attention layer handle.
  *   d_model   : model width D.
  *   dtype     : element type of x, W and out (MHA_BF16 or MHA_F32).

@@ -10,7 +10,8 @@ generators (``inputs``).  Attribute access loads the binding lazily, so
 importing the package (e.g. for ``inputs``) needs neither torch nor a GPU.
 """
 _BINDING_NAMES = {
-    "sdpa_forward", "sdpa_forward_host", "sdpa_decode", "decode_splits",
+    "sdpa_forward", "sdpa_forward_host", "sdpa_decode", "decode_splits", "sinusoidal_pe",
+    "embed_pe",
     "MASK_CAUSAL_BOTTOM_RIGHT", "mha_create", "mha_forward", "mha_check",
     "mha_destroy", "MhaHandle", "MhaError", "EncoderLayer", "EncoderParams",
     "ENCODER_PARAM_NAMES", "set_wait_limit_ms", "selftest_wait_timeout", "status_string", "lib",

@@ -60,6 +60,10 @@ def _declare(lib):
     lib.sdpa_decode.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, i32, vp, i32, i32,
                                 vp]
     lib.sdpa_decode.restype = i32
+    lib.sinusoidal_pe.argtypes = [vp, i32, i32, i32, vp]
+    lib.sinusoidal_pe.restype = i32
+    lib.embed_pe_forward.argtypes = [vp, vp, i32, vp, i32, vp, i32, i32, i32, i32, f32, i32, vp]
+    lib.embed_pe_forward.restype = i32
     lib.sdpa_decode_splits.argtypes = [i32, i32, i32, i32]
     lib.sdpa_decode_splits.restype = i32
     i64 = ctypes.c_int64
@@ -221,6 +225,39 @@ def sdpa_decode(Q, K_cache, V_cache, kv_lengths=None, causal: bool = True,
 def decode_splits(B: int, H: int, Lk: int, d: int) -> int:
     """The split count sdpa_decode picks by default."""
     return int(lib().sdpa_decode_splits(B, H, Lk, d))
+
+
+def sinusoidal_pe(n_pos: int, d_model: int, first_pos: int = 0, out=None, stream=None,
+                  device=None):
+    """The positional-encoding table, fp32 [n_pos, d_model] on the device."""
+    if out is None:
+        out = torch.empty((n_pos, d_model), dtype=torch.float32,
+                          device=device if device is not None else "cuda")
+    elif out.shape != (n_pos, d_model) or out.dtype != torch.float32:
+        raise ValueError("out has the wrong shape or dtype")
+    _check(lib().sinusoidal_pe(_dev_ptr(out), int(first_pos), int(n_pos), int(d_model),
+                               _stream(stream)), "sinusoidal_pe")
+    return out
+
+
+def embed_pe(ids, table, pe, pos_offset: int = 0, scale: float | None = None, out=None,
+             stream=None):
+    """x [B, L, D] = table[ids] * scale (default sqrt(D)) + pe[pos_offset + l]."""
+    B, L = ids.shape
+    vocab, D = table.shape
+    if ids.dtype != torch.int32:
+        raise ValueError("ids must be int32")
+    if pe.dtype != torch.float32 or pe.dim() != 2 or pe.shape[1] != D:
+        raise ValueError("pe must be float32 [rows, D]")
+    if out is None:
+        out = torch.empty((B, L, D), dtype=table.dtype, device=table.device)
+    elif out.shape != (B, L, D) or out.dtype != table.dtype:
+        raise ValueError("out has the wrong shape or dtype")
+    st = lib().embed_pe_forward(_dev_ptr(ids), _dev_ptr(table), vocab, _dev_ptr(pe), pe.shape[0],
+                                _dev_ptr(out), B, L, D, int(pos_offset), float(scale or 0.0),
+                                _dtype_code(table.dtype), _stream(stream))
+    _check(st, "embed_pe_forward")
+    return out
 
 
 class MhaHandle:

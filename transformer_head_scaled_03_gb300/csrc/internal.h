@@ -64,6 +64,14 @@ cudaError_t launch_add_layernorm(const void* a, const void* b, const void* gamma
                                  const void* beta, float eps, void* out, long M, int D,
                                  mha_dtype dt, cudaStream_t stream);
 
+// Device error bit of the embedding pass (ptx.cuh holds the others).
+constexpr unsigned kErrTokenId = 4u;  // a token id outside [0, vocab)
+
+cudaError_t launch_sinusoidal_pe(float* pe, int first_pos, int n_pos, int D, cudaStream_t s);
+cudaError_t launch_embed_pe(const int32_t* ids, const void* table, int vocab, const float* pe,
+                            void* x, long long rows, int L, int D, int pos_offset, float scale,
+                            mha_dtype dt, unsigned* err, cudaStream_t s);
+
 // One decode-shape attention launch (bf16 cache).
 struct DecodeArgs {
   const void* Q;  // [B, H, Lq, d]

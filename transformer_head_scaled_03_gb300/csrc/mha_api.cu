@@ -361,7 +361,7 @@ mha_status mha_check(mha_handle) {
       return MHA_ERR_CUDA;
   }
   if (word & kErrTimeout) return MHA_ERR_TIMEOUT;
-  if (word & kErrKeyLength) return MHA_ERR_DEVICE;
+  if (word & (kErrKeyLength | kErrTokenId)) return MHA_ERR_DEVICE;
   return MHA_OK;
 }
 
