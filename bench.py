@@ -120,13 +120,17 @@ def barrier():
 
 
 class ClockSampler:
-    """nvidia-smi clock/throttle samples every 20 ms while active.  Entering
-    waits (up to 3 s) for the sampler's first line, so sampling is live when
-    the timed region starts; only lines that arrive after that count."""
+    """SM clock and clock-event reasons while active: every 2 ms through the
+    driver's NVML library (read-only queries), so that timed regions of a
+    few milliseconds are covered too; nvidia-smi's 20 ms loop when NVML
+    cannot be loaded.  Only samples taken after entering count."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    # NVML clock-event reason bits (nvml.h)
+    NVML_REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+                    0x40: "hw_thermal_slowdown"}
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
@@ -134,8 +138,55 @@ class ClockSampler:
         self.lines = []
         self._t = None
         self._start = 0
+        self._nvml = None
+        self._stop = threading.Event()
+        self.samples = []   # (sm_mhz, max_mhz, reasons bitmask) from NVML
+
+    def _open_nvml(self):
+        import ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            return None
+        handle = ctypes.c_void_p()
+        ok = False
+        try:
+            import torch
+            uid = getattr(torch.cuda.get_device_properties(self.gpu), "uuid", None)
+            if uid is not None:
+                ok = lib.nvmlDeviceGetHandleByUUID(f"GPU-{uid}".encode(),
+                                                   ctypes.byref(handle)) == 0
+        except Exception:
+            ok = False
+        if not ok:
+            return None
+        reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        return lib, handle, reasons
+
+    def _poll_nvml(self):
+        import ctypes
+        lib, handle, reasons = self._nvml
+        clk, mx, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            if (lib.nvmlDeviceGetClockInfo(handle, 1, ctypes.byref(clk)) == 0 and
+                    lib.nvmlDeviceGetMaxClockInfo(handle, 1, ctypes.byref(mx)) == 0 and
+                    reasons(handle, ctypes.byref(rs)) == 0):
+                self.samples.append((clk.value, mx.value, rs.value))
+            time.sleep(0.002)
 
     def __enter__(self):
+        try:
+            self._nvml = self._open_nvml()
+        except Exception:
+            self._nvml = None
+        if self._nvml is not None:
+            self._t = threading.Thread(target=self._poll_nvml, daemon=True)
+            self._t.start()
+            t0 = time.perf_counter()
+            while not self.samples and time.perf_counter() - t0 < 1.0:
+                time.sleep(0.001)
+            self._start = len(self.samples)
+            return self
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
@@ -156,6 +207,11 @@ class ClockSampler:
             self.lines.append(line.strip())
 
     def __exit__(self, *exc):
+        if self._nvml is not None:
+            self._stop.set()
+            if self._t is not None:
+                self._t.join(timeout=2)
+            return
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -166,6 +222,16 @@ class ClockSampler:
                 self._t.join(timeout=2)
 
     def summary(self):
+        if self._nvml is not None:
+            got = self.samples[self._start:]
+            if not got:
+                return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                        "source": "nvml"}
+            reasons = sorted({name for _, _, bits in got
+                              for bit, name in self.NVML_REASONS.items() if bits & bit})
+            return {"sm_mhz": statistics.median(c for c, _, _ in got),
+                    "sm_max_mhz": max(m for _, m, _ in got), "reasons": reasons,
+                    "samples": len(got), "source": "nvml, 2 ms"}
         sms, maxes, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for ln in self.lines[self._start:]:
@@ -181,9 +247,10 @@ class ClockSampler:
                 if val.lower() == "active":
                     reasons.add(name)
         if not sms:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "source": "nvidia-smi"}
         return {"sm_mhz": statistics.median(sms), "sm_max_mhz": max(maxes),
-                "reasons": sorted(reasons), "samples": len(sms)}
+                "reasons": sorted(reasons), "samples": len(sms), "source": "nvidia-smi, 20 ms"}
 
 
 def oracle_cpu_baseline(w, Q, K, V, lens, rows):

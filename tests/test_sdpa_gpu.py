@@ -158,3 +158,28 @@ def test_empty_batch_is_a_no_op():
     Q = torch.empty((0, 2, 5, 64), dtype=torch.bfloat16, device="cuda")
     O = mha.sdpa_forward(Q, Q, Q)
     assert O.shape == (0, 2, 5, 64)
+
+
+# Shapes with more (b, h, query block) items than SMs and short key ranges:
+# the fused kernel runs one wave of CTAs that each work through a run of
+# items (the K/V ring, the Q buffers and every barrier phase carried from
+# one item to the next).  Causal runs mix block lengths; key padding gives
+# items of different lengths, including single-key and full-length ones.
+MULTI_ITEM_CASES = [
+    # B, H, Lq, Lk, d, mask, lengths
+    (40, 4, 700, 700, 64, CAUSAL, None),
+    (40, 4, 700, 700, 128, CAUSAL, None),
+    (24, 8, 300, 300, 64, PAD, None),
+    (30, 6, 513, 513, 128, PAD | CAUSAL, None),
+    (160, 1, 100, 1000, 64, NONE, None),       # one query tile per item
+    (20, 10, 256, 129, 128, PAD, [1] * 10 + [129] * 10),
+]
+
+
+@pytest.mark.parametrize("case", MULTI_ITEM_CASES, ids=[str(c[:6]) for c in MULTI_ITEM_CASES])
+def test_bf16_parity_several_items_per_cta(case):
+    B, H, Lq, Lk, d, mask, lengths = case
+    got, ref = run_case(500 + MULTI_ITEM_CASES.index(case), B, H, Lq, Lk, d, torch.bfloat16,
+                        mask, lengths)
+    max_abs, rms = assert_parity(got, ref, torch.bfloat16, str(case))
+    print(f"\n{case[:6]}: max|err| {max_abs:.3e} rms rel {rms:.3e}")

@@ -352,8 +352,7 @@ __global__ void __launch_bounds__(kThreads, DecCfg<D>::kCtasPerSm)
       if (!(ok = mbar_wait_warp(bar(C::bS(buf)), par, ctl))) break;
       tc_fence_after();
       uint32_t sr[kSlots];
-      tmem_ld16(tS + buf * kSlots, sr);
-      tmem_ld_wait(sr);
+      tmem_ld16_sync(tS + buf * kSlots, sr);
       const int key = (t_begin + j) * kKeys + r;
       float s[kSlots];
 #pragma unroll
@@ -414,8 +413,7 @@ __global__ void __launch_bounds__(kThreads, DecCfg<D>::kCtasPerSm)
         tc_fence_after();
         if (o_rows) {
           uint32_t orr[kSlots];
-          tmem_ld16(tO + (pj & 1) * kSlots, orr);
-          tmem_ld_wait(orr);
+          tmem_ld16_sync(tO + (pj & 1) * kSlots, orr);
 #pragma unroll
           for (int q = 0; q < kSlots; ++q)
             acc[q] = fmaf(acc[q], alpha_prev[q], __uint_as_float(orr[q]));
@@ -430,8 +428,7 @@ __global__ void __launch_bounds__(kThreads, DecCfg<D>::kCtasPerSm)
         tc_fence_after();
         if (o_rows) {
           uint32_t orr[kSlots];
-          tmem_ld16(tO + (pj & 1) * kSlots, orr);
-          tmem_ld_wait(orr);
+          tmem_ld16_sync(tO + (pj & 1) * kSlots, orr);
 #pragma unroll
           for (int q = 0; q < kSlots; ++q)
             acc[q] = fmaf(acc[q], alpha_prev[q], __uint_as_float(orr[q]));
