@@ -67,6 +67,8 @@ def _declare(lib):
     lib.oracle_encoder_layer.restype = c_int
     lib.oracle_encoder_layer_num_params.argtypes = [c_int, c_int]
     lib.oracle_encoder_layer_num_params.restype = ctypes.c_long
+    lib.oracle_sdpa_backward.argtypes = [dp] * 7 + [c_int] * 5 + [c_double, c_int, ip, c_int]
+    lib.oracle_sdpa_backward.restype = c_int
     lib.oracle_sinusoidal_pe.argtypes = [dp, c_int, c_int, c_int]
     lib.oracle_sinusoidal_pe.restype = None
     lib.oracle_embed_pe.argtypes = [ip, dp, c_int, dp, c_int, c_int, c_int, c_int, c_double]
@@ -245,6 +247,25 @@ def _embed_pe(self, ids, table, pos_offset: int = 0, scale: float = 0.0):
     return x
 
 
+def _sdpa_backward(self, Q, K, V, dO, scale: float = 0.0, mask_kind: int = MASK_NONE,
+                   key_lengths=None, nthreads: int = 0):
+    """Gradients (dQ, dK, dV) of sum(dO * sdpa(Q, K, V)) for Q [B,H,Lq,d],
+    K/V [B,H,Lk,d], dO [B,H,Lq,d]."""
+    Q, K, V, dO = _d(Q), _d(K), _d(V), _d(dO)
+    B, H, Lq, d = Q.shape
+    Lk = K.shape[2]
+    if K.shape != (B, H, Lk, d) or V.shape != (B, H, Lk, d) or dO.shape != Q.shape:
+        raise ValueError("shape mismatch")
+    dQ, dK, dV = np.empty_like(Q), np.empty_like(K), np.empty_like(V)
+    kl, klp = _lengths(mask_kind, key_lengths, B)
+    bad = self.lib.oracle_sdpa_backward(_ptr(Q), _ptr(K), _ptr(V), _ptr(dO), _ptr(dQ), _ptr(dK),
+                                        _ptr(dV), B, H, Lq, Lk, d, float(scale), int(mask_kind),
+                                        klp, int(nthreads))
+    self.last_bad_rows = int(bad)
+    return dQ, dK, dV
+
+
+Oracle.sdpa_backward = _sdpa_backward
 Oracle.sinusoidal_pe = _sinusoidal_pe
 Oracle.embed_pe = _embed_pe
 Oracle.encoder_layer = _encoder_layer
@@ -282,3 +303,7 @@ def sinusoidal_pe(*a, **k):
 
 def embed_pe(*a, **k):
     return default().embed_pe(*a, **k)
+
+
+def sdpa_backward(*a, **k):
+    return default().sdpa_backward(*a, **k)

@@ -428,6 +428,92 @@ long oracle_encoder_layer_num_params(int D, int F)
 }
 
 /*
+ * Gradient of scaled dot-product attention (the backward pass of training).
+ * Given dO = dL/dO for O = softmax(S) V with S = scale * Q K^T + M, the
+ * chain rule through the row softmax gives, per (b, h) and query row i:
+ *   P_ij  = softmax_j(S_ij)                  (the forward weights)
+ *   dV_j  = sum_i P_ij dO_i
+ *   dP_ij = <dO_i, V_j>
+ *   dS_ij = P_ij (dP_ij - sum_k P_ik dP_ik)  (softmax Jacobian)
+ *   dQ_i  = scale * sum_j dS_ij K_j
+ *   dK_j  = scale * sum_i dS_ij Q_i
+ * Training backpropagates through the attention formula of "How
+ * Transformers Work" (worksonmygpu.com), "Scaled dot-product attention";
+ * "32 Transformer" (ml-canon-en), "Why we divide by sqrt(dk)", discusses
+ * the gradient of this softmax (vanishing at inactive positions of a
+ * saturated row).  Masked keys have P = 0, so they receive no gradient.  A
+ * query row with no visible key has no defined softmax: its dQ row is NaN
+ * and it contributes nothing to dK and dV.  Returns the number of such
+ * rows.
+ */
+int oracle_sdpa_backward(const double *Q, const double *K, const double *V, const double *dO,
+                         double *dQ, double *dK, double *dV, int B, int H, int Lq, int Lk, int d,
+                         double scale, int mask_kind, const int32_t *key_lengths, int nthreads)
+{
+    const double sc = resolve_scale(scale, d);
+    int bad = 0;
+#ifdef _OPENMP
+    if (nthreads > 0)
+        omp_set_num_threads(nthreads);
+#endif
+    (void)nthreads;
+#pragma omp parallel for schedule(dynamic) reduction(+ : bad)
+    for (long bh = 0; bh < (long)B * H; ++bh) {
+        const int b = (int)(bh / H);
+        const int len_b = len_of(key_lengths, mask_kind, b, Lk);
+        const double *Qh = Q + (size_t)bh * Lq * d;
+        const double *Kh = K + (size_t)bh * Lk * d;
+        const double *Vh = V + (size_t)bh * Lk * d;
+        const double *dOh = dO + (size_t)bh * Lq * d;
+        double *dQh = dQ + (size_t)bh * Lq * d;
+        double *dKh = dK + (size_t)bh * Lk * d;
+        double *dVh = dV + (size_t)bh * Lk * d;
+        for (size_t e = 0; e < (size_t)Lk * d; ++e) {
+            dKh[e] = 0.0;
+            dVh[e] = 0.0;
+        }
+        const size_t n = (size_t)(Lk > 0 ? Lk : 1);
+        double *w = (double *)malloc(sizeof(double) * n);
+        double *dP = (double *)malloc(sizeof(double) * n);
+        double *o = (double *)malloc(sizeof(double) * (size_t)(d > 0 ? d : 1));
+        for (int i = 0; i < Lq; ++i) {
+            const double *q = Qh + (size_t)i * d;
+            const double *g = dOh + (size_t)i * d;
+            double *dq = dQh + (size_t)i * d;
+            if (attend_row(q, Kh, d, Vh, d, Lk, d, sc, i, Lq, mask_kind, len_b, NULL, w, o)) {
+                for (int c = 0; c < d; ++c)
+                    dq[c] = NAN;
+                ++bad;
+                continue;
+            }
+            /* dP_ij = <dO_i, V_j> and its P-weighted row mean */
+            double mean = 0.0;
+            for (int j = 0; j < Lk; ++j) {
+                double acc = 0.0;
+                for (int c = 0; c < d; ++c)
+                    acc += g[c] * Vh[(size_t)j * d + c];
+                dP[j] = acc;
+                mean += w[j] * acc;
+            }
+            for (int c = 0; c < d; ++c)
+                dq[c] = 0.0;
+            for (int j = 0; j < Lk; ++j) {
+                const double ds = w[j] * (dP[j] - mean);
+                for (int c = 0; c < d; ++c) {
+                    dq[c] += sc * ds * Kh[(size_t)j * d + c];
+                    dKh[(size_t)j * d + c] += sc * ds * q[c];
+                    dVh[(size_t)j * d + c] += w[j] * g[c];
+                }
+            }
+        }
+        free(w);
+        free(dP);
+        free(o);
+    }
+    return bad;
+}
+
+/*
  * Sinusoidal positional encoding, [n_pos, D] row-major:
  *   PE(pos, 2i)   = sin(pos / 10000^(2i / D))
  *   PE(pos, 2i+1) = cos(pos / 10000^(2i / D))

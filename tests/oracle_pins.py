@@ -30,6 +30,13 @@ Sources of the pinned facts:
     position"): "How Transformers Work" (worksonmygpu.com), "Positional
     encoding"; "The Transformer" (hoshank.vercel.app), "The Mathematics".
     The embedding lookup is cross-checked against torch's embedding.
+  - backward pass: torch's float64 autograd of scaled_dot_product_attention
+    (library routine); central finite differences of sum(dO * O); the
+    softmax-gradient structure (each row of dS sums to zero, so the key
+    gradients of a head sum to zero and the value gradients sum to the sum
+    of dO); blocked keys get no gradient; a saturated row's gradient
+    vanishes at its inactive positions ("32 Transformer" (ml-canon-en),
+    "Why we divide by sqrt(dk)").
   - decoding: the decoder sees earlier positions only and generates left to
     right, so attending from the last Lq positions against the cached keys
     and values reproduces those rows of the full causal pass: "How
@@ -570,6 +577,111 @@ def pin_decode_torch_lower_right(orc):
                                              attn_mask=causal_lower_right(Lq, Lk)).numpy()
         _allclose(orc.sdpa(Q, K, V, mask_kind=MASK_CAUSAL_BOTTOM_RIGHT), ref, 1e-12,
                   f"torch lower-right causal {B, H, Lq, Lk, d}")
+
+
+# ----------------------------------------------------------- backward pass
+
+def _torch_sdpa_grads(Q, K, V, dO, mask=None, scale=None):
+    import torch
+    import torch.nn.functional as F
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).requires_grad_(True)
+    q, k, v = t(Q), t(K), t(V)
+    o = F.scaled_dot_product_attention(q, k, v, attn_mask=mask, scale=scale)
+    o.backward(torch.from_numpy(dO))
+    return q.grad.numpy(), k.grad.numpy(), v.grad.numpy()
+
+
+def pin_backward_torch(orc):
+    """Library cross-check: torch float64 autograd, every mask kind."""
+    import torch
+    from torch.nn.attention.bias import causal_lower_right
+    rng = _rng(60)
+    B, H, Lq, Lk, d = 2, 3, 6, 9, 8
+    Q, K, V = _qkv(rng, B, H, Lq, Lk, d)
+    dO = rng.standard_normal(Q.shape)
+    for name, mk, lens, mask in (
+            ("none", MASK_NONE, None, None),
+            ("padding", MASK_KEY_PADDING, np.array([9, 3], np.int32),
+             torch.from_numpy(np.arange(Lk)[None, None, None, :] <
+                              np.array([9, 3])[:, None, None, None])),
+            ("bottom-right", MASK_CAUSAL_BOTTOM_RIGHT, None, causal_lower_right(Lq, Lk))):
+        got = orc.sdpa_backward(Q, K, V, dO, mask_kind=mk, key_lengths=lens)
+        ref = _torch_sdpa_grads(Q, K, V, dO, mask=mask)
+        for gname, a, b in zip(("dQ", "dK", "dV"), got, ref):
+            _allclose(a, b, 1e-12, f"torch {gname} {name}")
+    Qs, Ks, Vs = _qkv(rng, 1, 2, 7, 7, 8)
+    dOs = rng.standard_normal(Qs.shape)
+    got = orc.sdpa_backward(Qs, Ks, Vs, dOs, scale=0.7, mask_kind=MASK_CAUSAL)
+    causal = torch.from_numpy(np.tril(np.ones((7, 7), dtype=bool)))
+    ref = _torch_sdpa_grads(Qs, Ks, Vs, dOs, mask=causal, scale=0.7)
+    for gname, a, b in zip(("dQ", "dK", "dV"), got, ref):
+        _allclose(a, b, 1e-12, f"torch {gname} causal, scale 0.7")
+
+
+def pin_backward_finite_differences(orc):
+    """dL/dx for L = sum(dO * O) against central differences of the oracle's
+    own forward, entry by entry on a tiny head."""
+    rng = _rng(61)
+    Q, K, V = _qkv(rng, 1, 1, 3, 4, 3)
+    dO = rng.standard_normal(Q.shape)
+    dQ, dK, dV = orc.sdpa_backward(Q, K, V, dO, mask_kind=MASK_CAUSAL_BOTTOM_RIGHT)
+    loss = lambda q, k, v: float(np.sum(dO * orc.sdpa(q, k, v,
+                                                      mask_kind=MASK_CAUSAL_BOTTOM_RIGHT)))
+    eps = 1e-6
+    for which, grad in ((0, dQ), (1, dK), (2, dV)):
+        for idx in np.ndindex(grad.shape):
+            args_p = [Q.copy(), K.copy(), V.copy()]
+            args_m = [Q.copy(), K.copy(), V.copy()]
+            args_p[which][idx] += eps
+            args_m[which][idx] -= eps
+            fd = (loss(*args_p) - loss(*args_m)) / (2 * eps)
+            assert abs(fd - grad[idx]) < 1e-8, (which, idx, fd, grad[idx])
+
+
+def pin_backward_softmax_structure(orc):
+    """Each row of dS sums to zero: the key gradients of a head sum to zero,
+    shifting every key by one vector leaves dQ unchanged, and with every key
+    visible the value gradients sum to the sum of dO.  Blocked keys (beyond a
+    length, or later than a causal query) get exactly zero gradient."""
+    rng = _rng(62)
+    B, H, Lq, Lk, d = 2, 2, 5, 8, 6
+    Q, K, V = _qkv(rng, B, H, Lq, Lk, d)
+    dO = rng.standard_normal(Q.shape)
+    dQ, dK, dV = orc.sdpa_backward(Q, K, V, dO)
+    _allclose(dK.sum(axis=2), np.zeros((B, H, d)), 1e-12, "sum of dK")
+    _allclose(dV.sum(axis=2), dO.sum(axis=2), 1e-12, "sum of dV = sum of dO")
+    shift = rng.standard_normal(d)
+    _allclose(orc.sdpa_backward(Q, K + shift, V, dO)[0], dQ, 1e-11, "dQ under a key shift")
+    lens = np.array([3, 8], np.int32)
+    _, dKp, dVp = orc.sdpa_backward(Q, K, V, dO, mask_kind=MASK_KEY_PADDING, key_lengths=lens)
+    assert np.all(dKp[0, :, 3:] == 0.0) and np.all(dVp[0, :, 3:] == 0.0)
+    Qc, Kc, Vc = _qkv(rng, 1, 1, 6, 6, 4)
+    dOc = rng.standard_normal(Qc.shape)
+    dOc[:, :, 4:] = 0.0       # only queries 0..3 carry gradient
+    _, dKc, dVc = orc.sdpa_backward(Qc, Kc, Vc, dOc, mask_kind=MASK_CAUSAL)
+    assert np.all(dKc[:, :, 4:] == 0.0) and np.all(dVc[:, :, 4:] == 0.0)
+
+
+def pin_backward_saturation(orc):
+    """A row whose top score leads by a margin g is nearly one-hot, and the
+    gradient reaching its other keys shrinks like e^-g (the saturation that
+    scaling by 1/sqrt(dk) is there to avoid)."""
+    d, Lk = 4, 6
+    prev, prev_gap = None, None
+    for gap in (4.0, 8.0, 16.0):
+        Q = np.zeros((1, 1, 1, d))
+        Q[..., 0] = 1.0
+        K = np.zeros((1, 1, Lk, d))
+        K[..., 0, 0] = gap      # key 0 leads by gap in the scaled score
+        V = _rng(63).standard_normal((1, 1, Lk, d))
+        dO = np.ones((1, 1, 1, d))
+        _, dK, _ = orc.sdpa_backward(Q, K, V, dO, scale=1.0)
+        inactive = float(np.abs(dK[0, 0, 1:]).max())
+        assert inactive <= 4.0 * Lk * math.exp(-gap) * (np.abs(V).max() * d + 1.0)
+        if prev is not None:
+            # decays like e^-gap (up to the normaliser of the softmax)
+            assert inactive < 1.5 * prev * math.exp(-(gap - prev_gap))
+        prev, prev_gap = inactive, gap
 
 
 # ------------------------------------------------------ positional encoding

@@ -46,6 +46,13 @@ MUTANTS = [
     ("pe_offset_ignored", "const double pos = (double)(first_pos + r);",
      "const double pos = (double)(r);"),
     ("embed_not_scaled", "scale == 0.0 ? sqrt((double)D) : scale", "scale == 0.0 ? 1.0 : scale"),
+    ("bwd_ds_sign_flipped", "const double ds = w[j] * (dP[j] - mean);",
+     "const double ds = w[j] * (mean - dP[j]);"),
+    ("bwd_ds_no_mean", "const double ds = w[j] * (dP[j] - mean);", "const double ds = w[j] * dP[j];"),
+    ("bwd_dq_unscaled", "dq[c] += sc * ds * Kh[(size_t)j * d + c];", "dq[c] += ds * Kh[(size_t)j * d + c];"),
+    ("bwd_dv_uses_ds", "dVh[(size_t)j * d + c] += w[j] * g[c];", "dVh[(size_t)j * d + c] += w[j] * g[c] * sc;"),
+    ("bwd_dk_uses_key", "dKh[(size_t)j * d + c] += sc * ds * q[c];",
+     "dKh[(size_t)j * d + c] += sc * ds * Kh[(size_t)j * d + c];"),
     ("query_row_stride_wrong", "bad += attend_row(Qh + (size_t)i * d,",
      "bad += attend_row(Qh + (size_t)(Lq - 1 - i) * d,"),
 ]
