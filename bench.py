@@ -26,6 +26,8 @@ Extra legs in the same JSON line:
   decode       sdpa_decode (Lq new queries against a bf16 key/value cache,
                bottom-right causal) on the three decode workloads, in GB/s
                of cache streamed against the measured HBM peak
+  backward     sdpa_backward (dQ, dK, dV) on the long-context and decoder
+               causal shapes, in TFLOP/s (2.5x the forward's flops)
   cpu_baseline the fp64 oracle on this host's cores on a bounded row sample
 
 Multi-GPU: the path has no exchange step, so N ranks run N replicas (one per
@@ -755,6 +757,50 @@ def bench_embed_pe(shape, steps, warmup, local_rank, hbm_peak, layer_shape=None)
     return out
 
 
+def bench_backward(w, steps, warmup, local_rank, peak):
+    """sdpa_backward (dQ, dK, dV of a causal or unmasked SDPA) in TFLOP/s.
+
+    Algorithmic flops are 2.5x the forward's: five products over the visible
+    (query, key) pairs (S recomputed, dP, dV, dK, dQ), 2 d flops each.  Each
+    call is the whole public call: the D = rowsum(dO * O) pass, the dQ zero
+    fill and the fused kernel.  Inputs are N(0, 1) bf16 drawn on the device,
+    larger than L2, and O and lse come from sdpa_forward_lse outside the
+    timed region."""
+    import torch
+    import transformer_head_scaled_03_gb300 as mha
+
+    dev = torch.device("cuda", local_rank)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(0x5EED0500 + w.wid)
+    mk = lambda L: torch.randn(w.B, w.H, L, w.d, generator=gen, device=dev).to(torch.bfloat16)
+    Q, K, V, dO = mk(w.Lq), mk(w.Lk), mk(w.Lk), mk(w.Lq)
+    O, lse = mha.sdpa_forward_lse(Q, K, V, mask_kind=w.mask)
+    ws = torch.empty(max(16, w.B * w.H * w.Lq * 4), dtype=torch.uint8, device=dev)
+    grads = mha.sdpa_backward(Q, K, V, O, dO, lse, mask_kind=w.mask, workspace=ws)
+    dQ, dK, dV = grads
+    for _ in range(warmup):
+        mha.sdpa_backward(Q, K, V, O, dO, lse, mask_kind=w.mask, workspace=ws)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        mha.sdpa_backward(Q, K, V, O, dO, lse, mask_kind=w.mask, workspace=ws)
+    e1.record()
+    torch.cuda.synchronize()
+    st = mha.mha_check()
+    if st != mha.MHA_OK:
+        raise RuntimeError(mha.status_string(st))
+    ms = e0.elapsed_time(e1) / steps
+    flops = 2.5 * w.flops()
+    tf = flops / (ms / 1e3) / 1e12
+    del Q, K, V, dO, O, lse, dQ, dK, dV, grads, ws
+    torch.cuda.empty_cache()
+    return {"workload": w.name, "mask": {0: "none", 1: "causal"}[w.mask],
+            "ms_per_call": round(ms, 4), "flops_per_call": flops, "tflops": round(tf, 2),
+            "frac_of_peak": round(tf / peak, 4), "peak": peak, "grad_dtype": "bf16 dK dV, fp32 dQ",
+            "gpu_launches_per_call": 2, "timing": "eager, CUDA events, inputs > L2"}
+
+
 def _time_eager_and_graph(step, steps, warmup):
     """(eager ms, CUDA-graph-replay ms) per call of ``step``."""
     import torch
@@ -826,6 +872,11 @@ def run_gpu(args):
         decode = [bench_decode(WORKLOADS[i], 50, 5, local_rank, peaks["hbm_gbs"])
                   for i in (6, 7, 8)]
 
+    backward = None
+    if not args.skip_backward:
+        backward = [bench_backward(WORKLOADS[5], 5, 3, local_rank, peaks["bf16_tflops"]),
+                    bench_backward(WORKLOADS[3], 20, 3, local_rank, peaks["bf16_tflops"])]
+
     cpu = None
     if rank == 0 and not args.skip_cpu:
         # about 10 s of fp64 oracle work on a 16-core host
@@ -879,6 +930,7 @@ def run_gpu(args):
         "encoder_layer": encoder_layer,
         "embed_pe": embed,
         "decode": decode,
+        "backward": backward,
     }
     print(json.dumps(line), flush=True)
     if world > 1:
@@ -984,6 +1036,7 @@ def main(argv=None):
     ap.add_argument("--skip-mha", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--skip-decode", action="store_true")
+    ap.add_argument("--skip-backward", action="store_true")
     ap.add_argument("--cpu-rows-per-head", type=int, default=None,
                     help="oracle CPU-baseline sample (default: about 10 s of work)")
     ap.add_argument("--ref-rows-per-head", type=int, default=4)

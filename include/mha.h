@@ -38,6 +38,7 @@
 #ifndef GB300_MHA_H
 #define GB300_MHA_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -158,6 +159,51 @@ mha_status sdpa_decode(const void *Q, const void *K_cache, const void *V_cache,
 
 /* The split count sdpa_decode uses for num_splits = 0 (0 for bad sizes). */
 int sdpa_decode_splits(int B, int H, int Lk, int d);
+
+/*
+ * sdpa_forward_lse -- sdpa_forward (bf16 inputs) that also writes, per query
+ * row, the base-2 log-sum-exp of the scaled scores, which the backward pass
+ * needs to recompute the attention weights:
+ *   lse[b, h, i] = log2( sum_j 2^((scale * <Q_i, K_j> + M_ij) * log2(e)) )
+ * (+inf for a row with no visible key).
+ *   lse : device fp32 [B, H, Lq], 4-byte aligned, caller-owned.
+ * Other arguments, layouts, support and errors as for sdpa_forward with
+ * in_dtype = MHA_BF16.
+ */
+mha_status sdpa_forward_lse(const void *Q, const void *K, const void *V, void *O,
+                            float *lse, int B, int H, int Lq, int Lk, int d,
+                            float scale, int mask_kind,
+                            const int32_t *key_lengths, mha_dtype out_dtype,
+                            mha_stream stream);
+
+/* Workspace sdpa_backward needs, in bytes (one fp32 per query row). */
+size_t sdpa_backward_workspace_bytes(int B, int H, int Lq);
+
+/*
+ * sdpa_backward -- gradients of scaled dot-product attention (the training
+ * step through the attention formula of "How Transformers Work"
+ * (worksonmygpu.com), "Scaled dot-product attention"): given dO = dL/dO for
+ * O = sdpa_forward(Q, K, V),
+ *   dV = P^T dO,  dS = P * (dO V^T - rowsum(dO * O)),
+ *   dQ = scale * dS K,  dK = scale * dS^T Q.
+ *   Q, O, dO [B, H, Lq, d] bf16; K, V [B, H, Lk, d] bf16 (as in the forward).
+ *   lse     : fp32 [B, H, Lq] from sdpa_forward_lse on the same inputs.
+ *   dQ      : fp32 [B, H, Lq, d] (written: zeroed, then accumulated).
+ *   dK, dV  : [B, H, Lk, d] of grad_dtype (MHA_BF16 or MHA_F32).
+ *   scale, mask_kind, key_lengths : as in the forward (CAUSAL and
+ *             KEY_PADDING; no float mask).
+ *   workspace : device, >= sdpa_backward_workspace_bytes(B, H, Lq) bytes.
+ * d must be 64 or 128; all pointers 16-byte aligned.  Blocked keys receive
+ * zero gradient.  The call allocates nothing.
+ * Returns MHA_OK, MHA_ERR_INVALID_ARG, MHA_ERR_UNSUPPORTED or MHA_ERR_CUDA.
+ */
+mha_status sdpa_backward(const void *Q, const void *K, const void *V,
+                         const void *O, const void *dO, const float *lse,
+                         float *dQ, void *dK, void *dV, int B, int H, int Lq,
+                         int Lk, int d, float scale, int mask_kind,
+                         const int32_t *key_lengths, mha_dtype grad_dtype,
+                         void *workspace, size_t workspace_bytes,
+                         mha_stream stream);
 
 /*
  * sinusoidal_pe -- the positional-encoding table, fp32 [n_pos, d_model]:

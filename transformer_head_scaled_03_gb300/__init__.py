@@ -11,6 +11,7 @@ importing the package (e.g. for ``inputs``) needs neither torch nor a GPU.
 """
 _BINDING_NAMES = {
     "sdpa_forward", "sdpa_forward_host", "sdpa_decode", "decode_splits", "sinusoidal_pe",
+    "sdpa_forward_lse", "sdpa_backward",
     "embed_pe",
     "MASK_CAUSAL_BOTTOM_RIGHT", "mha_create", "mha_forward", "mha_check",
     "mha_destroy", "MhaHandle", "MhaError", "EncoderLayer", "EncoderParams",

@@ -60,6 +60,14 @@ def _declare(lib):
     lib.sdpa_decode.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, i32, vp, i32, i32,
                                 vp]
     lib.sdpa_decode.restype = i32
+    lib.sdpa_forward_lse.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, i32, vp,
+                                     i32, vp]
+    lib.sdpa_forward_lse.restype = i32
+    lib.sdpa_backward_workspace_bytes.argtypes = [i32, i32, i32]
+    lib.sdpa_backward_workspace_bytes.restype = ctypes.c_size_t
+    lib.sdpa_backward.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
+                                  f32, i32, vp, i32, vp, ctypes.c_size_t, vp]
+    lib.sdpa_backward.restype = i32
     lib.sinusoidal_pe.argtypes = [vp, i32, i32, i32, vp]
     lib.sinusoidal_pe.restype = i32
     lib.embed_pe_forward.argtypes = [vp, vp, i32, vp, i32, vp, i32, i32, i32, i32, f32, i32, vp]
@@ -225,6 +233,47 @@ def sdpa_decode(Q, K_cache, V_cache, kv_lengths=None, causal: bool = True,
 def decode_splits(B: int, H: int, Lk: int, d: int) -> int:
     """The split count sdpa_decode picks by default."""
     return int(lib().sdpa_decode_splits(B, H, Lk, d))
+
+
+def sdpa_forward_lse(Q, K, V, scale: float | None = None, mask_kind: int = MASK_NONE,
+                     key_lengths=None, out=None, lse=None, stream=None):
+    """bf16 forward that also returns the base-2 row log-sum-exp [B,H,Lq]."""
+    B, H, Lq, d = Q.shape
+    Lk = K.shape[2]
+    if Q.dtype != torch.bfloat16 or K.dtype != Q.dtype or V.dtype != Q.dtype:
+        raise ValueError("bf16 Q/K/V required")
+    if out is None:
+        out = torch.empty_like(Q)
+    if lse is None:
+        lse = torch.empty((B, H, Lq), dtype=torch.float32, device=Q.device)
+    st = lib().sdpa_forward_lse(_dev_ptr(Q), _dev_ptr(K), _dev_ptr(V), _dev_ptr(out),
+                                _dev_ptr(lse), B, H, Lq, Lk, d, float(scale or 0.0),
+                                int(mask_kind), _dev_ptr(key_lengths), _dtype_code(out.dtype),
+                                _stream(stream))
+    _check(st, "sdpa_forward_lse")
+    return out, lse
+
+
+def sdpa_backward(Q, K, V, O, dO, lse, scale: float | None = None, mask_kind: int = MASK_NONE,
+                  key_lengths=None, grad_dtype: torch.dtype = torch.bfloat16, workspace=None,
+                  stream=None):
+    """(dQ fp32, dK, dV) of scaled dot-product attention for upstream dO."""
+    B, H, Lq, d = Q.shape
+    Lk = K.shape[2]
+    dQ = torch.empty((B, H, Lq, d), dtype=torch.float32, device=Q.device)
+    dK = torch.empty((B, H, Lk, d), dtype=grad_dtype, device=Q.device)
+    dV = torch.empty((B, H, Lk, d), dtype=grad_dtype, device=Q.device)
+    need = int(lib().sdpa_backward_workspace_bytes(B, H, Lq))
+    if workspace is None:
+        workspace = torch.empty(max(16, (need + 15) // 16 * 16), dtype=torch.uint8,
+                                device=Q.device)
+    st = lib().sdpa_backward(_dev_ptr(Q), _dev_ptr(K), _dev_ptr(V), _dev_ptr(O), _dev_ptr(dO),
+                             _dev_ptr(lse), _dev_ptr(dQ), _dev_ptr(dK), _dev_ptr(dV), B, H, Lq, Lk,
+                             d, float(scale or 0.0), int(mask_kind), _dev_ptr(key_lengths),
+                             _dtype_code(grad_dtype), _dev_ptr(workspace),
+                             workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "sdpa_backward")
+    return dQ, dK, dV
 
 
 def sinusoidal_pe(n_pos: int, d_model: int, first_pos: int = 0, out=None, stream=None,

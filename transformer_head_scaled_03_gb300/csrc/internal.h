@@ -26,6 +26,9 @@ struct SdpaArgs {
   // add_mask[b*mask_sb + h*mask_sh + i*Lk + j]; nullptr when absent
   const float* add_mask;
   int64_t mask_sb, mask_sh;
+  // optional: per query row the base-2 log-sum-exp of the scaled scores,
+  // [B, H, Lq] fp32 (bf16 path only); nullptr when not wanted
+  float* lse = nullptr;
 };
 
 // Row-major GEMM C = A[M,K] @ W[K,N] with a choice of store layout.

@@ -1,0 +1,600 @@
+// sdpa_backward.cu -- the backward pass of scaled dot-product attention
+// (training), bf16 in, fp32 accumulate, on sm_103a tcgen05 tensor cores.
+//
+// Given dO = dL/dO for O = softmax(S) V, S = scale Q K^T + M, and the row
+// log-sum-exp of the forward pass (lse, base 2):
+//   P    = 2^(S log2(e) - lse)               recomputed per tile
+//   dV  += P^T dO
+//   dP   = dO V^T
+//   dS   = P (dP - D),  D_i = <dO_i, O_i>    (= sum_j P_ij dP_ij)
+//   dK  += scale dS^T Q
+//   dQ  += scale dS K
+// (the chain rule through the attention formula of "How Transformers Work"
+// (worksonmygpu.com), "Scaled dot-product attention"; the softmax gradient
+// "32 Transformer" (ml-canon-en), "Why we divide by sqrt(dk)", discusses).
+//
+// CTA = one tile of 128 keys of one (b, h); it walks the query tiles that
+// can see those keys and keeps dK and dV in tensor memory throughout.  In
+// transposed form, with keys on the MMA's M side (TMEM lanes):
+//   S^T  = K Q^T        M 128 keys, N 128 queries, K = d      TMEM cols 0-127
+//   dP^T = V dO^T       same shape                            TMEM cols 128-255
+//   P^T  -> bf16 over S^T's first 64 columns; dS^T -> bf16 over dP^T's
+//   dV  += P^T dO       A = P^T from TMEM, B = dO (MN-major)  TMEM dV
+//   dK  += dS^T Q       A = dS^T from TMEM, B = Q (MN-major)  TMEM dK
+//   dQ_t = dS K         A = dS in shared memory (MN-major, written by the
+//                       softmax threads), B = K (MN-major)   TMEM cols 0..d-1
+// and the dQ tile is added to an fp32 dQ accumulator in global memory (the
+// key tiles of a head all contribute to every query row).
+//
+// Warps 0-3 compute P, dS and move dQ (one TMEM lane each: a key for S^T
+// and dP^T, a query for the dQ tile), warp 4 loads (TMA), warp 5 issues the
+// MMAs.  Every wait is bounded.
+#include <math.h>
+#include <stdint.h>
+
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+#include "ptx_cluster.cuh"
+
+namespace mha {
+namespace {
+
+constexpr int kTile = 128;       // keys per CTA = queries per step
+constexpr int kSub = 16384;      // one 128-row x 64-column bf16 box
+constexpr int kThreads = 192;
+constexpr int kLoadWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr uint32_t kTmemCols = 512;
+
+template <int D>
+struct BwdCfg {
+  static_assert(D == 64 || D == 128, "head dim");
+  static constexpr int KB = D / 64;
+  static constexpr int kTileBytes = KB * kSub;   // a 128-row tile of K, V, Q or dO
+  static constexpr int NST = D == 128 ? 2 : 3;    // Q/dO stages
+  // shared memory from a 1024-byte aligned base
+  static constexpr int kOffK = 0;
+  static constexpr int kOffV = kOffK + kTileBytes;
+  static constexpr int kOffQ = kOffV + kTileBytes;                 // NST stages
+  static constexpr int kOffDO = kOffQ + NST * kTileBytes;          // NST stages
+  static constexpr int kOffDS = kOffDO + NST * kTileBytes;         // dS, 2 x 64 queries
+  static constexpr int kOffBar = kOffDS + 2 * kSub;
+  // barriers
+  static constexpr int bKV = 0;
+  __host__ __device__ static constexpr int bFull(int s) { return 1 + s; }
+  __host__ __device__ static constexpr int bEmpty(int s) { return 1 + NST + s; }
+  static constexpr int bS = 1 + 2 * NST;
+  static constexpr int bDP = bS + 1;
+  static constexpr int bP = bS + 2;
+  static constexpr int bDS = bS + 3;
+  static constexpr int bDQ = bS + 4;
+  static constexpr int bDQR = bS + 5;
+  static constexpr int bFinal = bS + 6;
+  static constexpr int bDrain = bS + 7;
+  static constexpr int kNumBars = bDrain + 1;
+  static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
+  static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
+  static_assert(kSmemBytes <= 232448, "shared memory");
+  // tensor memory
+  static constexpr uint32_t tS = 0, tDP = 128, tDV = 256, tDK = 256 + D;
+};
+
+struct BwdParams {
+  const float* lse;     // [B, H, Lq], base 2
+  const float* dsum;    // [B, H, Lq], D_i = <dO_i, O_i>
+  float* dq;            // [B, H, Lq, d] fp32 accumulator (zeroed by the caller)
+  void* dk;             // [B, H, Lk, d]
+  void* dv;
+  int B, H, Lq, Lk;
+  int num_k_tiles;
+  int mask_kind;
+  const int32_t* key_lengths;
+  float scale;
+  float scale_log2;
+  int out_f32;
+  unsigned* err;
+  uint64_t limit_ns;
+};
+
+__device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_timer_ns() - t0 > limit_ns) return;
+  }
+}
+
+// Four fp32 adds to global memory in one reduction (no return value).
+__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b),
+               "f"(c), "f"(d)
+               : "memory");
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    sdpa_bwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ,
+                         const __grid_constant__ CUtensorMap tmK,
+                         const __grid_constant__ CUtensorMap tmV,
+                         const __grid_constant__ CUtensorMap tmDO, const BwdParams p) {
+  using C = BwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + C::kOffMisc);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kOffMisc + 4);
+  auto bar = [base](int i) -> uint32_t { return base + C::kOffBar + 8u * i; };
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const WaitCtl ctl{abort_flag, p.err, p.limit_ns};
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(C::bKV), 1);
+    for (int s = 0; s < C::NST; ++s) {
+      mbar_init(bar(C::bFull(s)), 1);
+      mbar_init(bar(C::bEmpty(s)), 1);
+    }
+    mbar_init(bar(C::bS), 1);
+    mbar_init(bar(C::bDP), 1);
+    mbar_init(bar(C::bP), 128);
+    mbar_init(bar(C::bDS), 128);
+    mbar_init(bar(C::bDQ), 1);
+    mbar_init(bar(C::bDQR), 128);
+    mbar_init(bar(C::bFinal), 1);
+    mbar_init(bar(C::bDrain), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc<kTmemCols>(smem_u32(tmem_slot));
+    tmem_relinquish();
+  }
+  if (warp == kLoadWarp && lane == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+    tma_prefetch_desc(&tmDO);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+
+  // ---- this CTA's (b, h) and key tile: head-major, so the CTAs resident at
+  // once share a head's Q and dO in L2; causal key tiles go from the first
+  // (which sees the most query tiles) to the last.
+  const bool causal = (p.mask_kind & MHA_MASK_CAUSAL) != 0;
+  const bool padded = (p.mask_kind & MHA_MASK_KEY_PADDING) != 0;
+  const int bh = static_cast<int>(blockIdx.x) / p.num_k_tiles;
+  const int kt = static_cast<int>(blockIdx.x) - bh * p.num_k_tiles;
+  const int b = bh / p.H;
+  const int k0 = kt * kTile;
+  int len = p.Lk;
+  bool bad_len = false;
+  if (padded) {
+    len = __ldg(p.key_lengths + b);
+    if (len < 1 || len > p.Lk) bad_len = true;
+  }
+  if (bad_len && kt == 0 && threadIdx.x == 0) atomicOr(p.err, kErrKeyLength);
+  const int n_qt_all = (p.Lq + kTile - 1) / kTile;
+  const int qt_begin = causal ? k0 / kTile : 0;
+  const int n_qt = (bad_len || k0 >= len) ? 0 : max(0, n_qt_all - qt_begin);
+
+  if (warp == kLoadWarp) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0 && n_qt > 0) {
+      mbar_expect_tx(bar(C::bKV), 2 * C::kTileBytes);
+      for (int kb = 0; kb < C::KB; ++kb) {
+        tma_load_3d(base + C::kOffK + kb * kSub, &tmK, bar(C::bKV), kb * 64, k0, bh);
+        tma_load_3d(base + C::kOffV + kb * kSub, &tmV, bar(C::bKV), kb * 64, k0, bh);
+      }
+      int issued = 0;
+      for (int j = 0; j < n_qt; ++j) {
+        const int st = j % C::NST;
+        const uint32_t ph = (j / C::NST) & 1;
+        if (!mbar_wait(bar(C::bEmpty(st)), ph ^ 1u, ctl)) break;
+        const int q0 = (qt_begin + j) * kTile;
+        mbar_expect_tx(bar(C::bFull(st)), 2 * C::kTileBytes);
+        for (int kb = 0; kb < C::KB; ++kb) {
+          tma_load_3d(base + C::kOffQ + st * C::kTileBytes + kb * kSub, &tmQ, bar(C::bFull(st)),
+                      kb * 64, q0, bh);
+          tma_load_3d(base + C::kOffDO + st * C::kTileBytes + kb * kSub, &tmDO,
+                      bar(C::bFull(st)), kb * 64, q0, bh);
+        }
+        issued = j + 1;
+      }
+      wait_drain(bar(C::bKV), 0, p.limit_ns);
+      for (int j = max(0, issued - C::NST); j < issued; ++j)
+        wait_drain(bar(C::bFull(j % C::NST)), (j / C::NST) & 1, p.limit_ns);
+    }
+  } else if (warp == kMmaWarp) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0 && n_qt > 0) {
+      constexpr uint32_t kIdT = idesc_bf16_f32(kTile, kTile, false, false);   // S^T, dP^T
+      constexpr uint32_t kIdG = idesc_bf16_f32(kTile, D, false, true);       // dV, dK
+      constexpr uint32_t kIdQ = idesc_bf16_f32(kTile, D, true, true);        // dQ
+      const uint64_t k_desc = sdesc_sw128(base + C::kOffK, 16, 1024);
+      const uint64_t v_desc = sdesc_sw128(base + C::kOffV, 16, 1024);
+      const uint64_t k_mn = sdesc_sw128(base + C::kOffK, kSub, 1024);
+      const uint64_t q_desc = sdesc_sw128(base + C::kOffQ, 16, 1024);
+      const uint64_t q_mn = sdesc_sw128(base + C::kOffQ, kSub, 1024);
+      const uint64_t do_desc = sdesc_sw128(base + C::kOffDO, 16, 1024);
+      const uint64_t do_mn = sdesc_sw128(base + C::kOffDO, kSub, 1024);
+      const uint64_t ds_mn = sdesc_sw128(base + C::kOffDS, kSub, 1024);
+      // D-step products of 128-row tiles along d: 16 elements = 32 bytes in
+      // a 128-byte row, 64-column blocks kSub apart
+      auto issue_t = [&](uint32_t d_tmem, uint64_t a, uint64_t bd) {
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint64_t off = static_cast<uint64_t>(((ks >> 2) * kSub + (ks & 3) * 32) >> 4);
+          umma_ss(d_tmem, a + off, bd + off, kIdT, ks > 0 ? 1u : 0u);
+        }
+      };
+      // products over the 128 queries (or keys) of a tile: A from TMEM
+      // (16 bf16 = 8 columns per step), B MN-major (16 rows of 128 bytes)
+      auto issue_g = [&](uint32_t d_tmem, uint32_t a_tmem, uint64_t bd, uint32_t accumulate) {
+#pragma unroll
+        for (int ks = 0; ks < kTile / 16; ++ks)
+          umma_ts(d_tmem, a_tmem + ks * 8, bd + static_cast<uint64_t>((ks * 16 * 128) >> 4),
+                  kIdG, ks > 0 ? 1u : accumulate);
+      };
+      bool ok = mbar_wait(bar(C::bKV), 0, ctl);
+      for (int j = 0; ok && j < n_qt; ++j) {
+        const int st = j % C::NST;
+        const uint32_t ph = (j / C::NST) & 1;
+        const uint32_t par = j & 1;
+        const uint64_t soff = static_cast<uint64_t>((st * C::kTileBytes) >> 4);
+        if (!(ok = mbar_wait(bar(C::bFull(st)), ph, ctl))) break;
+        // S^T reuses the columns of the previous dQ tile once it was read
+        if (j > 0 && !(ok = mbar_wait(bar(C::bDQR), par ^ 1u, ctl))) break;
+        tc_fence_after();
+        issue_t(tmem + C::tS, k_desc, q_desc + soff);
+        umma_commit(bar(C::bS));
+        issue_t(tmem + C::tDP, v_desc, do_desc + soff);
+        umma_commit(bar(C::bDP));
+        if (!(ok = mbar_wait(bar(C::bP), par, ctl))) break;
+        tc_fence_after();
+        issue_g(tmem + C::tDV, tmem + C::tS, do_mn + soff, j > 0 ? 1u : 0u);
+        if (!(ok = mbar_wait(bar(C::bDS), par, ctl))) break;
+        tc_fence_after();
+        issue_g(tmem + C::tDK, tmem + C::tDP, q_mn + soff, j > 0 ? 1u : 0u);
+        // dQ tile = dS K: both operands MN-major in shared memory, 16 keys
+        // (16 rows of 128 bytes) per step; it overwrites P^T, which the dV
+        // product above has read (MMAs execute in issue order)
+#pragma unroll
+        for (int ks = 0; ks < kTile / 16; ++ks) {
+          const uint64_t off = static_cast<uint64_t>((ks * 16 * 128) >> 4);
+          umma_ss(tmem + C::tS, ds_mn + off, k_mn + off, kIdQ, ks > 0 ? 1u : 0u);
+        }
+        umma_commit(bar(C::bDQ));
+        umma_commit(bar(C::bEmpty(st)));
+      }
+      umma_commit(bar(C::bFinal));
+      umma_commit(bar(C::bDrain));
+      wait_drain(bar(C::bDrain), 0, p.limit_ns);
+    }
+  } else {
+    // ------------------------------------------------------ compute warps
+    const int L = warp * 32 + lane;  // TMEM lane: key k0 + L, or query q0 + L
+    const uint32_t lane_bits = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t tl = tmem + lane_bits;
+    const int key = k0 + L;
+    const bool key_live = key < len;
+    const float sl2 = p.scale_log2;
+    const float* lse_h = p.lse + static_cast<size_t>(bh) * p.Lq;
+    const float* dsum_h = p.dsum + static_cast<size_t>(bh) * p.Lq;
+    uint8_t* ds_s = gbase + C::kOffDS;
+    // 4 consecutive row values as one float4 only when every row of the head
+    // starts 16-byte aligned (Lq % 4 == 0; the base is 16-byte aligned);
+    // past Lq the value is `fill`
+    const bool vec4 = (p.Lq & 3) == 0;
+    auto load4 = [&](const float* row, int q, float fill) -> float4 {
+      if (vec4 && q + 3 < p.Lq) return __ldg(reinterpret_cast<const float4*>(row + q));
+      return make_float4(q < p.Lq ? __ldg(row + q) : fill, q + 1 < p.Lq ? __ldg(row + q + 1) : fill,
+                         q + 2 < p.Lq ? __ldg(row + q + 2) : fill,
+                         q + 3 < p.Lq ? __ldg(row + q + 3) : fill);
+    };
+    bool ok = true;
+    for (int j = 0; j < n_qt; ++j) {
+      const uint32_t par = j & 1;
+      const int q0 = (qt_begin + j) * kTile;
+      // ---- P^T row of this key over the tile's 128 queries
+      if (!(ok = mbar_wait_warp(bar(C::bS), par, ctl))) break;
+      tc_fence_after();
+      float pr[kTile];
+      {
+        uint32_t s[kTile];
+        tmem_ld32(tl + C::tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
+        tmem_ld32(tl + C::tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
+        tmem_ld32(tl + C::tS + 64, *reinterpret_cast<uint32_t(*)[32]>(&s[64]));
+        tmem_ld32(tl + C::tS + 96, *reinterpret_cast<uint32_t(*)[32]>(&s[96]));
+        tmem_ld_wait(s);
+#pragma unroll
+        for (int c = 0; c < kTile; c += 4) {
+          const int q = q0 + c;
+          // lse = +inf for queries past Lq (and rows with no visible key)
+          const float4 lv = load4(lse_h, q, INFINITY);
+          const float lq[4] = {lv.x, lv.y, lv.z, lv.w};
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const bool vis = key_live && (!causal || key <= q + u);
+            pr[c + u] = vis ? ex2_approx(fmaf(__uint_as_float(s[c + u]), sl2, -lq[u])) : 0.f;
+          }
+        }
+        uint32_t pk[kTile / 2];
+#pragma unroll
+        for (int c = 0; c < kTile / 2; ++c) pk[c] = pack_bf16x2(pr[2 * c], pr[2 * c + 1]);
+        tmem_st32(tl + C::tS + 0, *reinterpret_cast<const uint32_t(*)[32]>(&pk[0]));
+        tmem_st32(tl + C::tS + 32, *reinterpret_cast<const uint32_t(*)[32]>(&pk[32]));
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(C::bP));
+      // ---- dS^T = P^T (dP^T - D), 32 queries at a time; bf16 into TMEM
+      // over dP^T (columns already read) and into shared memory as the
+      // MN-major A operand of the dQ product (row = key, 64-query blocks)
+      if (!(ok = mbar_wait_warp(bar(C::bDP), par, ctl))) break;
+      tc_fence_after();
+      // the dQ product of the previous tile has read dS from shared memory:
+      // its completion (bDQ of j - 1) was awaited before the dQ readback
+#pragma unroll
+      for (int cc = 0; cc < kTile / 32; ++cc) {
+        uint32_t dp[32];
+        tmem_ld32(tl + C::tDP + cc * 32, dp);
+        tmem_ld_wait(dp);
+        uint32_t dsk[16];
+#pragma unroll
+        for (int i = 0; i < 32; i += 4) {
+          const int q = q0 + cc * 32 + i;
+          const float4 dv = load4(dsum_h, q, 0.f);
+          const float ds0 = pr[cc * 32 + i] * (__uint_as_float(dp[i]) - dv.x);
+          const float ds1 = pr[cc * 32 + i + 1] * (__uint_as_float(dp[i + 1]) - dv.y);
+          const float ds2 = pr[cc * 32 + i + 2] * (__uint_as_float(dp[i + 2]) - dv.z);
+          const float ds3 = pr[cc * 32 + i + 3] * (__uint_as_float(dp[i + 3]) - dv.w);
+          dsk[i / 2] = pack_bf16x2(ds0, ds1);
+          dsk[i / 2 + 1] = pack_bf16x2(ds2, ds3);
+        }
+        // TMEM: 32 queries of bf16 = 16 columns at 128 + 16 cc (inside the
+        // dP^T columns this thread has already loaded)
+        asm volatile(
+            "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+            "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(
+                tl + C::tDP + cc * 16),
+            "r"(dsk[0]), "r"(dsk[1]), "r"(dsk[2]), "r"(dsk[3]), "r"(dsk[4]), "r"(dsk[5]),
+            "r"(dsk[6]), "r"(dsk[7]), "r"(dsk[8]), "r"(dsk[9]), "r"(dsk[10]), "r"(dsk[11]),
+            "r"(dsk[12]), "r"(dsk[13]), "r"(dsk[14]), "r"(dsk[15])
+            : "memory");
+        // shared memory: queries [32 cc, 32 cc + 32) of row L, in block
+        // (32 cc) / 64, 16-byte chunks ((q % 64) / 8) ^ (L % 8)
+        uint8_t* row = ds_s + ((cc * 32) / 64) * kSub + (L >> 3) * 1024 + (L & 7) * 128;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int chunk = (((cc * 32) & 63) >> 3) + u;
+          *reinterpret_cast<uint4*>(row + ((chunk ^ (L & 7)) << 4)) =
+              make_uint4(dsk[4 * u], dsk[4 * u + 1], dsk[4 * u + 2], dsk[4 * u + 3]);
+        }
+      }
+      tmem_st_wait();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(bar(C::bDS));
+      // ---- dQ tile (lane = query q0 + L): scale, add into the fp32 dQ
+      if (!(ok = mbar_wait_warp(bar(C::bDQ), par, ctl))) break;
+      tc_fence_after();
+      const int q = q0 + L;
+      float* dq_row = p.dq + (static_cast<size_t>(bh) * p.Lq + q) * D;
+#pragma unroll
+      for (int cb = 0; cb < D / 32; ++cb) {
+        uint32_t g[32];
+        tmem_ld32(tl + C::tS + cb * 32, g);
+        tmem_ld_wait(g);
+        if (q < p.Lq) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 4)
+            red_add_v4(dq_row + cb * 32 + i, __uint_as_float(g[i]) * p.scale,
+                       __uint_as_float(g[i + 1]) * p.scale, __uint_as_float(g[i + 2]) * p.scale,
+                       __uint_as_float(g[i + 3]) * p.scale);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(bar(C::bDQR));
+    }
+    // ---- epilogue: dV and scale dK for this key
+    bool have = ok && n_qt > 0;
+    if (have) {
+      have = mbar_wait_warp(bar(C::bFinal), 0, ctl);
+      tc_fence_after();
+    }
+    // tcgen05.ld is warp-collective: the whole warp loads (have is uniform
+    // across the warp), and only the stores are limited to keys below Lk
+    {
+      const size_t row = (static_cast<size_t>(bh) * p.Lk + key) * D;
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        const uint32_t col = which == 0 ? C::tDV : C::tDK;
+        const float mul = which == 0 ? 1.f : p.scale;
+        void* out = which == 0 ? p.dv : p.dk;
+#pragma unroll
+        for (int cb = 0; cb < D / 32; ++cb) {
+          uint32_t g[32];
+          if (have) {
+            tmem_ld32(tl + col + cb * 32, g);
+            tmem_ld_wait(g);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) g[i] = 0u;
+          }
+          if (key >= p.Lk) continue;
+          if (p.out_f32) {
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out) + row + cb * 32);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              dst[i] = make_float4(__uint_as_float(g[4 * i]) * mul, __uint_as_float(g[4 * i + 1]) * mul,
+                                   __uint_as_float(g[4 * i + 2]) * mul,
+                                   __uint_as_float(g[4 * i + 3]) * mul);
+          } else {
+            uint4* dst =
+                reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out) + row + cb * 32);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              dst[i] = make_uint4(
+                  pack_bf16x2(__uint_as_float(g[8 * i]) * mul, __uint_as_float(g[8 * i + 1]) * mul),
+                  pack_bf16x2(__uint_as_float(g[8 * i + 2]) * mul, __uint_as_float(g[8 * i + 3]) * mul),
+                  pack_bf16x2(__uint_as_float(g[8 * i + 4]) * mul, __uint_as_float(g[8 * i + 5]) * mul),
+                  pack_bf16x2(__uint_as_float(g[8 * i + 6]) * mul, __uint_as_float(g[8 * i + 7]) * mul));
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kMmaWarp) tmem_dealloc<kTmemCols>(tmem);
+}
+
+// D_i = <dO_i, O_i> for every query row: one warp per row, fp32 sum.
+template <int D>
+__global__ void __launch_bounds__(256) bwd_rowdot_kernel(const __nv_bfloat16* __restrict__ dO,
+                                                         const __nv_bfloat16* __restrict__ O,
+                                                         float* __restrict__ dsum, long long rows) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (long long r = static_cast<long long>(blockIdx.x) * 8 + warp; r < rows;
+       r += static_cast<long long>(gridDim.x) * 8) {
+    const __nv_bfloat162* a = reinterpret_cast<const __nv_bfloat162*>(dO + r * D);
+    const __nv_bfloat162* c = reinterpret_cast<const __nv_bfloat162*>(O + r * D);
+    float acc = 0.f;
+#pragma unroll
+    for (int i = lane; i < D / 2; i += 32) {
+      const float2 x = __bfloat1622float2(__ldg(a + i));
+      const float2 y = __bfloat1622float2(__ldg(c + i));
+      acc = fmaf(x.x, y.x, fmaf(x.y, y.y, acc));
+    }
+#pragma unroll
+    for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
+    if (lane == 0) dsum[r] = acc;
+  }
+}
+
+template <int D>
+cudaError_t launch_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                       const float* lse, float* dsum, float* dq, void* dk, void* dv, int B, int H,
+                       int Lq, int Lk, float scale, int mask_kind, const int32_t* key_lengths,
+                       bool out_f32, const DeviceCtl& ctl, cudaStream_t stream) {
+  using C = BwdCfg<D>;
+  const long long rows = static_cast<long long>(B) * H * Lq;
+  int sms = 148, dev = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess)
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const long long want = (rows + 7) / 8;
+  const int blocks = static_cast<int>(want < 16LL * sms ? want : 16LL * sms);
+  bwd_rowdot_kernel<D><<<blocks, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(dO),
+                                                    static_cast<const __nv_bfloat16*>(O), dsum,
+                                                    rows);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  e = cudaMemsetAsync(dq, 0, static_cast<size_t>(rows) * D * sizeof(float), stream);
+  if (e != cudaSuccess) return e;
+  CUtensorMap maps[4];
+  const void* ptrs[4] = {Q, K, V, dO};
+  const int lens[4] = {Lq, Lk, Lk, Lq};
+  for (int i = 0; i < 4; ++i) {
+    const uint64_t dims[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(lens[i]),
+                              static_cast<uint64_t>(B) * H};
+    const uint64_t strides[2] = {static_cast<uint64_t>(D) * 2,
+                                 static_cast<uint64_t>(lens[i]) * D * 2};
+    const uint32_t box[3] = {64, kTile, 1};
+    if (!encode_tensor_map(&maps[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                           const_cast<void*>(ptrs[i]), dims, strides, box,
+                           CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  }
+  BwdParams p;
+  p.lse = lse;
+  p.dsum = dsum;
+  p.dq = dq;
+  p.dk = dk;
+  p.dv = dv;
+  p.B = B;
+  p.H = H;
+  p.Lq = Lq;
+  p.Lk = Lk;
+  p.num_k_tiles = (Lk + kTile - 1) / kTile;
+  p.mask_kind = mask_kind;
+  p.key_lengths = key_lengths;
+  p.scale = scale;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  p.out_f32 = out_f32 ? 1 : 0;
+  p.err = ctl.err;
+  p.limit_ns = ctl.limit_ns;
+  const long long grid = static_cast<long long>(p.num_k_tiles) * B * H;
+  if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  auto kern = sdpa_bwd_bf16_kernel<D>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  kern<<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(maps[0], maps[1],
+                                                                         maps[2], maps[3], p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+}  // namespace mha
+
+using namespace mha;
+
+extern "C" {
+
+mha_status sdpa_forward_lse(const void* Q, const void* K, const void* V, void* O, float* lse,
+                            int B, int H, int Lq, int Lk, int d, float scale, int mask_kind,
+                            const int32_t* key_lengths, mha_dtype out_dtype, mha_stream stream) {
+  const mha_status st = validate_sdpa(Q, K, V, O, B, H, Lq, Lk, d, scale, mask_kind,
+                                      key_lengths, MHA_BF16, out_dtype);
+  if (st != MHA_OK) return st;
+  if (static_cast<long long>(B) * H * Lq == 0) return MHA_OK;
+  if (!lse || (reinterpret_cast<uintptr_t>(lse) & 3u)) return MHA_ERR_INVALID_ARG;
+  DeviceCtl ctl;
+  if (!device_ctl(&ctl)) return MHA_ERR_CUDA;
+  SdpaArgs a{Q, K, V, O, B, H, Lq, Lk, d,
+             scale == 0.f ? static_cast<float>(1.0 / sqrt(static_cast<double>(d))) : scale,
+             mask_kind, key_lengths, MHA_BF16, out_dtype, false,
+             reinterpret_cast<cudaStream_t>(stream), nullptr, 0, 0, lse};
+  const cudaError_t e = launch_sdpa_bf16(a, ctl);
+  return e == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
+}
+
+size_t sdpa_backward_workspace_bytes(int B, int H, int Lq) {
+  if (B < 0 || H < 0 || Lq < 0) return 0;
+  return static_cast<size_t>(B) * H * Lq * sizeof(float);
+}
+
+mha_status sdpa_backward(const void* Q, const void* K, const void* V, const void* O,
+                         const void* dO, const float* lse, float* dQ, void* dK, void* dV, int B,
+                         int H, int Lq, int Lk, int d, float scale, int mask_kind,
+                         const int32_t* key_lengths, mha_dtype grad_dtype, void* workspace,
+                         size_t workspace_bytes, mha_stream stream) {
+  const mha_status st = validate_sdpa(Q, K, V, O, B, H, Lq, Lk, d, scale, mask_kind,
+                                      key_lengths, MHA_BF16, MHA_BF16);
+  if (st != MHA_OK) return st;
+  if (grad_dtype != MHA_BF16 && grad_dtype != MHA_F32) return MHA_ERR_INVALID_ARG;
+  if (static_cast<long long>(B) * H * (Lq + Lk) == 0) return MHA_OK;
+  const void* ptrs[6] = {dO, dQ, dK, dV, lse, workspace};
+  for (const void* ptr : ptrs)
+    if (!ptr || (reinterpret_cast<uintptr_t>(ptr) & 15u)) return MHA_ERR_INVALID_ARG;
+  if (workspace_bytes < sdpa_backward_workspace_bytes(B, H, Lq)) return MHA_ERR_INVALID_ARG;
+  DeviceCtl ctl;
+  if (!device_ctl(&ctl)) return MHA_ERR_CUDA;
+  const float sc = scale == 0.f ? static_cast<float>(1.0 / sqrt(static_cast<double>(d))) : scale;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  float* dsum = static_cast<float*>(workspace);
+  const cudaError_t e =
+      d == 64 ? launch_bwd<64>(Q, K, V, O, dO, lse, dsum, dQ, dK, dV, B, H, Lq, Lk, sc, mask_kind,
+                               key_lengths, grad_dtype == MHA_F32, ctl, s)
+              : launch_bwd<128>(Q, K, V, O, dO, lse, dsum, dQ, dK, dV, B, H, Lq, Lk, sc,
+                                mask_kind, key_lengths, grad_dtype == MHA_F32, ctl, s);
+  return e == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
+}
+
+}  // extern "C"

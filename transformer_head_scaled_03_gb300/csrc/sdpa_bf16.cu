@@ -56,6 +56,7 @@ struct SdpaParams {
   int64_t mask_sb, mask_sh;
   float inv_scale;        // the mask is added to raw scores as M / scale
   int mask_vec;           // rows are 16-byte aligned: load the mask as float4
+  float* lse;             // optional [B, H, Lq]: log2 of sum_j 2^(s_ij * scale_log2)
 };
 
 template <int D, int NQT, int NST>
@@ -103,7 +104,7 @@ __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, uint64
   }
 }
 
-template <int D, int NQT, int NST, bool kAddMask>
+template <int D, int NQT, int NST, bool kAddMask, bool kLse>
 __global__ void __launch_bounds__(Cfg<D, NQT, NST>::kThreads, 1)
     sdpa_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ,
                          const __grid_constant__ CUtensorMap tmK,
@@ -421,6 +422,15 @@ __global__ void __launch_bounds__(Cfg<D, NQT, NST>::kThreads, 1)
       tc_fence_after();
     }
     const float inv_l = (have && l > 0.f) ? 1.f / l : 0.f;
+    // The backward pass recomputes P = 2^(s * scale_log2 - lse) from this:
+    // with p = 2^((s - m_ref) * scale_log2) summing to l, the row's
+    // log-sum-exp (base 2) is m_ref * scale_log2 + log2(l); +inf for a row
+    // with no visible key, so that its P is 0.
+    if constexpr (kLse) {
+      if (q_row < p.Lq)
+        p.lse[static_cast<size_t>(bh) * p.Lq + q_row] =
+            (have && l > 0.f) ? fmaf(m_ref, sl2, log2f(l)) : INFINITY;
+    }
     const size_t row_idx = p.ctx_layout
                                ? (static_cast<size_t>(b) * p.Lq + q_row) * p.H + h
                                : static_cast<size_t>(bh) * p.Lq + q_row;
@@ -470,7 +480,7 @@ __global__ void __launch_bounds__(Cfg<D, NQT, NST>::kThreads, 1)
   if (warp == C::kMmaWarp) tmem_dealloc<C::kTmemCols>(tmem);
 }
 
-template <int D, int NQT, int NST, bool kAddMask>
+template <int D, int NQT, int NST, bool kAddMask, bool kLse = false>
 cudaError_t launch_impl(const SdpaArgs& a, const DeviceCtl& ctl) {
   using C = Cfg<D, NQT, NST>;
   CUtensorMap maps[3];
@@ -505,12 +515,13 @@ cudaError_t launch_impl(const SdpaArgs& a, const DeviceCtl& ctl) {
   p.mask_sb = a.mask_sb;
   p.mask_sh = a.mask_sh;
   p.inv_scale = 1.f / a.scale;
+  p.lse = a.lse;
   p.mask_vec = a.add_mask && (reinterpret_cast<uintptr_t>(a.add_mask) & 15u) == 0 &&
                a.Lk % 4 == 0 && a.mask_sb % 4 == 0 && a.mask_sh % 4 == 0;
   const long long grid = static_cast<long long>(p.num_q_blocks) * a.B * a.H;
   if (grid <= 0) return cudaSuccess;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  auto kern = sdpa_fwd_bf16_kernel<D, NQT, NST, kAddMask>;
+  auto kern = sdpa_fwd_bf16_kernel<D, NQT, NST, kAddMask, kLse>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
@@ -531,6 +542,17 @@ cudaError_t launch_sdpa_bf16(const SdpaArgs& a, const DeviceCtl& ctl) {
       return two ? launch_impl<64, 2, 3, true>(a, ctl) : launch_impl<64, 1, 3, true>(a, ctl);
     if (a.d == 128)
       return two ? launch_impl<128, 2, 2, true>(a, ctl) : launch_impl<128, 1, 2, true>(a, ctl);
+    return cudaErrorInvalidValue;
+  }
+  // the row log-sum-exp store is a separate instantiation, so the plain
+  // forward's code is unchanged by it
+  if (a.lse != nullptr) {
+    if (a.d == 64)
+      return two ? launch_impl<64, 2, 3, false, true>(a, ctl)
+                 : launch_impl<64, 1, 3, false, true>(a, ctl);
+    if (a.d == 128)
+      return two ? launch_impl<128, 2, 2, false, true>(a, ctl)
+                 : launch_impl<128, 1, 2, false, true>(a, ctl);
     return cudaErrorInvalidValue;
   }
   if (a.d == 64)
