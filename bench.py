@@ -874,8 +874,10 @@ def run_gpu(args):
 
     backward = None
     if not args.skip_backward:
-        backward = [bench_backward(WORKLOADS[5], 5, 3, local_rank, peaks["bf16_tflops"]),
-                    bench_backward(WORKLOADS[3], 20, 3, local_rank, peaks["bf16_tflops"])]
+        # the selected shape (no mask or causal), then the decoder causal shape
+        shapes = [w] if (w.mask in (0, 1) and w.wid != 3) else []
+        backward = [bench_backward(x, 5 if x.Lq >= 16384 else 20, 3, local_rank,
+                                   peaks["bf16_tflops"]) for x in shapes + [WORKLOADS[3]]]
 
     cpu = None
     if rank == 0 and not args.skip_cpu:

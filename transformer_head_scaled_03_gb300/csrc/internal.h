@@ -67,8 +67,10 @@ cudaError_t launch_add_layernorm(const void* a, const void* b, const void* gamma
                                  const void* beta, float eps, void* out, long M, int D,
                                  mha_dtype dt, cudaStream_t stream);
 
-// Device error bit of the embedding pass (ptx.cuh holds the others).
-constexpr unsigned kErrTokenId = 4u;  // a token id outside [0, vocab)
+// Device error bits of the embedding pass and the backward pass (ptx.cuh
+// holds the others).
+constexpr unsigned kErrTokenId = 4u;     // a token id outside [0, vocab)
+constexpr unsigned kErrSmemLayout = 8u;  // dynamic shared memory too misaligned for the layout
 
 cudaError_t launch_sinusoidal_pe(float* pe, int first_pos, int n_pos, int D, cudaStream_t s);
 cudaError_t launch_embed_pe(const int32_t* ids, const void* table, int vocab, const float* pe,

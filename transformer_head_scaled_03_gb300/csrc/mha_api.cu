@@ -361,7 +361,7 @@ mha_status mha_check(mha_handle) {
       return MHA_ERR_CUDA;
   }
   if (word & kErrTimeout) return MHA_ERR_TIMEOUT;
-  if (word & (kErrKeyLength | kErrTokenId)) return MHA_ERR_DEVICE;
+  if (word) return MHA_ERR_DEVICE;  // key length, token id, shared-memory layout
   return MHA_OK;
 }
 

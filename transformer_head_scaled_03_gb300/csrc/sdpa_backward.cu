@@ -13,22 +13,29 @@
 // (worksonmygpu.com), "Scaled dot-product attention"; the softmax gradient
 // "32 Transformer" (ml-canon-en), "Why we divide by sqrt(dk)", discusses).
 //
-// CTA = one tile of 128 keys of one (b, h); it walks the query tiles that
-// can see those keys and keeps dK and dV in tensor memory throughout.  In
-// transposed form, with keys on the MMA's M side (TMEM lanes):
+// CTA = one tile of 128 keys of one (b, h); it walks the 128-query tiles
+// that can see those keys and keeps dK and dV in tensor memory throughout.
+// Keys sit on the MMA's M side (TMEM lanes):
 //   S^T  = K Q^T        M 128 keys, N 128 queries, K = d      TMEM cols 0-127
 //   dP^T = V dO^T       same shape                            TMEM cols 128-255
-//   P^T  -> bf16 over S^T's first 64 columns; dS^T -> bf16 over dP^T's
+//   P^T  -> bf16 over S^T's first 64 columns, in two halves of 64 queries
+//   dS^T -> bf16 over dP^T's first 64 columns, and into shared memory
 //   dV  += P^T dO       A = P^T from TMEM, B = dO (MN-major)  TMEM dV
 //   dK  += dS^T Q       A = dS^T from TMEM, B = Q (MN-major)  TMEM dK
-//   dQ_t = dS K         A = dS in shared memory (MN-major, written by the
-//                       softmax threads), B = K (MN-major)   TMEM cols 0..d-1
-// and the dQ tile is added to an fp32 dQ accumulator in global memory (the
-// key tiles of a head all contribute to every query row).
+//   dQ^T = K^T dS^T     A = K (MN-major), B = dS^T (MN-major, the shared
+//                       copy): M = d on the TMEM lanes (d = 64 pads M to 128
+//                       with rows that are never read), N 128 queries;
+//                       d = 128 writes it over dP^T, d = 64 into cols 384-511
+// and the dQ tile is added to an fp32 dQ accumulator in global memory: a
+// warp's lanes hold 32 consecutive d of one query row, so each reduction
+// instruction covers 128 contiguous bytes.
 //
-// Warps 0-3 compute P, dS and move dQ (one TMEM lane each: a key for S^T
-// and dP^T, a query for the dQ tile), warp 4 loads (TMA), warp 5 issues the
-// MMAs.  Every wait is bounded.
+// Warps 0-3 compute P and dS (one key per TMEM lane), warps 4-7 move the dQ
+// tile out (one d per lane) and write dK at the end, warp 8 loads (TMA, and
+// the tile's lse and D rows into shared memory), warp 9 issues the MMAs in
+// the order dV(j), S^T(j+1), dK(j), dQ^T(j), dP^T(j+1), so the next tile's
+// exponentials run under this tile's dK and dQ products.  Every wait is
+// bounded.
 #include <math.h>
 #include <stdint.h>
 
@@ -43,10 +50,12 @@ namespace {
 
 constexpr int kTile = 128;       // keys per CTA = queries per step
 constexpr int kSub = 16384;      // one 128-row x 64-column bf16 box
-constexpr int kThreads = 192;
-constexpr int kLoadWarp = 4;
-constexpr int kMmaWarp = 5;
+constexpr int kThreads = 320;
+constexpr int kDqWarp0 = 4;      // warps 4-7
+constexpr int kLoadWarp = 8;
+constexpr int kMmaWarp = 9;
 constexpr uint32_t kTmemCols = 512;
+constexpr int kMaxSmem = 232448;  // per-CTA opt-in limit
 
 template <int D>
 struct BwdCfg {
@@ -60,25 +69,33 @@ struct BwdCfg {
   static constexpr int kOffQ = kOffV + kTileBytes;                 // NST stages
   static constexpr int kOffDO = kOffQ + NST * kTileBytes;          // NST stages
   static constexpr int kOffDS = kOffDO + NST * kTileBytes;         // dS, 2 x 64 queries
-  static constexpr int kOffBar = kOffDS + 2 * kSub;
+  static constexpr int kOffRow = kOffDS + 2 * kSub;                // NST x {lse[128], D[128]}
+  static constexpr int kOffBar = kOffRow + NST * 1024;
   // barriers
   static constexpr int bKV = 0;
   __host__ __device__ static constexpr int bFull(int s) { return 1 + s; }
   __host__ __device__ static constexpr int bEmpty(int s) { return 1 + NST + s; }
-  static constexpr int bS = 1 + 2 * NST;
-  static constexpr int bDP = bS + 1;
-  static constexpr int bP = bS + 2;
-  static constexpr int bDS = bS + 3;
-  static constexpr int bDQ = bS + 4;
-  static constexpr int bDQR = bS + 5;
-  static constexpr int bFinal = bS + 6;
-  static constexpr int bDrain = bS + 7;
+  static constexpr int bS = 1 + 2 * NST;   // S^T(j) complete
+  static constexpr int bDP = bS + 1;       // dP^T(j) complete
+  static constexpr int bP0 = bS + 2;       // P^T(j) queries 0-63 in TMEM
+  static constexpr int bP1 = bS + 3;       // P^T(j) queries 64-127 in TMEM
+  static constexpr int bDS = bS + 4;       // dS(j) in TMEM and shared memory
+  static constexpr int bDQ = bS + 5;       // dQ^T(j) complete
+  static constexpr int bDQF = bS + 6;      // dQ^T(j) read out of TMEM
+  static constexpr int bFinal = bS + 7;
+  static constexpr int bDrain = bS + 8;
   static constexpr int kNumBars = bDrain + 1;
   static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
-  static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
-  static_assert(kSmemBytes <= 232448, "shared memory");
+  static constexpr int kUsed = kOffMisc + 16;   // bytes from the aligned base
+  static_assert(kUsed <= kMaxSmem, "shared memory");
+  // the allocation leaves room to align the base; d = 128 has 896 bytes of
+  // slack (the dynamic window starts 1024-byte aligned in practice, and the
+  // kernel checks)
+  static constexpr int kSmemBytes = kUsed + 1024 <= kMaxSmem ? kUsed + 1024 : kMaxSmem;
   // tensor memory
   static constexpr uint32_t tS = 0, tDP = 128, tDV = 256, tDK = 256 + D;
+  static constexpr bool kDqOverDp = D == 128;
+  static constexpr uint32_t tDQ = kDqOverDp ? tDP : 384;
 };
 
 struct BwdParams {
@@ -105,11 +122,55 @@ __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, uint64
   }
 }
 
-// Four fp32 adds to global memory in one reduction (no return value).
-__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b),
-               "f"(c), "f"(d)
-               : "memory");
+__device__ __forceinline__ void red_add_f32(float* addr, float v) {
+  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
+}
+
+// 4 consecutive values of a per-row array from row q on; `fill` past Lq.
+// One float4 only when every head's row starts 16-byte aligned (Lq % 4 == 0).
+__device__ __forceinline__ float4 load_row4(const float* row, int q, int Lq, float fill) {
+  if ((Lq & 3) == 0 && q + 3 < Lq) return __ldg(reinterpret_cast<const float4*>(row + q));
+  return make_float4(q < Lq ? __ldg(row + q) : fill, q + 1 < Lq ? __ldg(row + q + 1) : fill,
+                     q + 2 < Lq ? __ldg(row + q + 2) : fill, q + 3 < Lq ? __ldg(row + q + 3) : fill);
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
+
+// dK or dV of this thread's key from TMEM (whole warp; zeros when `have` is
+// false), times `mul`, stored for key < Lk.
+template <int D>
+__device__ __forceinline__ void store_key_grad(uint32_t taddr, bool have, float mul, void* out,
+                                               size_t row, bool live, bool f32) {
+#pragma unroll
+  for (int cb = 0; cb < D / 32; ++cb) {
+    uint32_t g[32];
+    if (have) {
+      tmem_ld32(taddr + cb * 32, g);
+      tmem_ld_wait(g);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) g[i] = 0u;
+    }
+    if (!live) continue;
+    if (f32) {
+      float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out) + row + cb * 32);
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        dst[i] = make_float4(__uint_as_float(g[4 * i]) * mul, __uint_as_float(g[4 * i + 1]) * mul,
+                             __uint_as_float(g[4 * i + 2]) * mul,
+                             __uint_as_float(g[4 * i + 3]) * mul);
+    } else {
+      uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out) + row + cb * 32);
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        dst[i] = make_uint4(
+            pack_bf16x2(__uint_as_float(g[8 * i]) * mul, __uint_as_float(g[8 * i + 1]) * mul),
+            pack_bf16x2(__uint_as_float(g[8 * i + 2]) * mul, __uint_as_float(g[8 * i + 3]) * mul),
+            pack_bf16x2(__uint_as_float(g[8 * i + 4]) * mul, __uint_as_float(g[8 * i + 5]) * mul),
+            pack_bf16x2(__uint_as_float(g[8 * i + 6]) * mul, __uint_as_float(g[8 * i + 7]) * mul));
+    }
+  }
 }
 
 template <int D>
@@ -122,6 +183,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
+  if (base - raw + C::kUsed > static_cast<uint32_t>(C::kSmemBytes)) {
+    // before any barrier or TMEM allocation: the whole CTA leaves
+    if (threadIdx.x == 0) atomicOr(p.err, kErrSmemLayout);
+    return;
+  }
   uint8_t* gbase = smem_raw + (base - raw);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + C::kOffMisc);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kOffMisc + 4);
@@ -138,10 +204,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(bar(C::bS), 1);
     mbar_init(bar(C::bDP), 1);
-    mbar_init(bar(C::bP), 128);
+    mbar_init(bar(C::bP0), 128);
+    mbar_init(bar(C::bP1), 128);
     mbar_init(bar(C::bDS), 128);
     mbar_init(bar(C::bDQ), 1);
-    mbar_init(bar(C::bDQR), 128);
+    mbar_init(bar(C::bDQF), 128);
     mbar_init(bar(C::bFinal), 1);
     mbar_init(bar(C::bDrain), 1);
     *abort_flag = 0;
@@ -184,47 +251,62 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kLoadWarp) {
     // ------------------------------------------------------------ producer
-    if (lane == 0 && n_qt > 0) {
-      mbar_expect_tx(bar(C::bKV), 2 * C::kTileBytes);
-      for (int kb = 0; kb < C::KB; ++kb) {
-        tma_load_3d(base + C::kOffK + kb * kSub, &tmK, bar(C::bKV), kb * 64, k0, bh);
-        tma_load_3d(base + C::kOffV + kb * kSub, &tmV, bar(C::bKV), kb * 64, k0, bh);
+    if (n_qt > 0) {
+      if (lane == 0) {
+        mbar_expect_tx(bar(C::bKV), 2 * C::kTileBytes);
+        for (int kb = 0; kb < C::KB; ++kb) {
+          tma_load_3d(base + C::kOffK + kb * kSub, &tmK, bar(C::bKV), kb * 64, k0, bh);
+          tma_load_3d(base + C::kOffV + kb * kSub, &tmV, bar(C::bKV), kb * 64, k0, bh);
+        }
       }
+      const float* lse_h = p.lse + static_cast<size_t>(bh) * p.Lq;
+      const float* dsum_h = p.dsum + static_cast<size_t>(bh) * p.Lq;
       int issued = 0;
       for (int j = 0; j < n_qt; ++j) {
         const int st = j % C::NST;
         const uint32_t ph = (j / C::NST) & 1;
-        if (!mbar_wait(bar(C::bEmpty(st)), ph ^ 1u, ctl)) break;
+        if (!mbar_wait_warp(bar(C::bEmpty(st)), ph ^ 1u, ctl)) break;
         const int q0 = (qt_begin + j) * kTile;
-        mbar_expect_tx(bar(C::bFull(st)), 2 * C::kTileBytes);
-        for (int kb = 0; kb < C::KB; ++kb) {
-          tma_load_3d(base + C::kOffQ + st * C::kTileBytes + kb * kSub, &tmQ, bar(C::bFull(st)),
-                      kb * 64, q0, bh);
-          tma_load_3d(base + C::kOffDO + st * C::kTileBytes + kb * kSub, &tmDO,
-                      bar(C::bFull(st)), kb * 64, q0, bh);
+        // the tile's lse (+inf past Lq, so P = 0 there) and D rows, 4 per lane
+        float4* rows = reinterpret_cast<float4*>(gbase + C::kOffRow + st * 1024);
+        rows[lane] = load_row4(lse_h, q0 + 4 * lane, p.Lq, INFINITY);
+        rows[32 + lane] = load_row4(dsum_h, q0 + 4 * lane, p.Lq, 0.f);
+        __syncwarp();  // the lanes' stores precede lane 0's arrive (a release)
+        if (lane == 0) {
+          mbar_expect_tx(bar(C::bFull(st)), 2 * C::kTileBytes);
+          for (int kb = 0; kb < C::KB; ++kb) {
+            tma_load_3d(base + C::kOffQ + st * C::kTileBytes + kb * kSub, &tmQ,
+                        bar(C::bFull(st)), kb * 64, q0, bh);
+            tma_load_3d(base + C::kOffDO + st * C::kTileBytes + kb * kSub, &tmDO,
+                        bar(C::bFull(st)), kb * 64, q0, bh);
+          }
         }
         issued = j + 1;
       }
-      wait_drain(bar(C::bKV), 0, p.limit_ns);
-      for (int j = max(0, issued - C::NST); j < issued; ++j)
-        wait_drain(bar(C::bFull(j % C::NST)), (j / C::NST) & 1, p.limit_ns);
+      if (lane == 0) {
+        wait_drain(bar(C::bKV), 0, p.limit_ns);
+        for (int j = max(0, issued - C::NST); j < issued; ++j)
+          wait_drain(bar(C::bFull(j % C::NST)), (j / C::NST) & 1, p.limit_ns);
+      }
     }
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0 && n_qt > 0) {
       constexpr uint32_t kIdT = idesc_bf16_f32(kTile, kTile, false, false);   // S^T, dP^T
       constexpr uint32_t kIdG = idesc_bf16_f32(kTile, D, false, true);       // dV, dK
-      constexpr uint32_t kIdQ = idesc_bf16_f32(kTile, D, true, true);        // dQ
+      constexpr uint32_t kIdQ = idesc_bf16_f32(kTile, kTile, true, true);    // dQ^T
       const uint64_t k_desc = sdesc_sw128(base + C::kOffK, 16, 1024);
       const uint64_t v_desc = sdesc_sw128(base + C::kOffV, 16, 1024);
-      const uint64_t k_mn = sdesc_sw128(base + C::kOffK, kSub, 1024);
+      // K^T as the MN-major A of dQ^T: M = d in 64-element blocks kSub apart
+      // (for d = 64 the second block is the V tile: rows never read)
+      const uint64_t kt_mn = sdesc_sw128(base + C::kOffK, kSub, 1024);
       const uint64_t q_desc = sdesc_sw128(base + C::kOffQ, 16, 1024);
       const uint64_t q_mn = sdesc_sw128(base + C::kOffQ, kSub, 1024);
       const uint64_t do_desc = sdesc_sw128(base + C::kOffDO, 16, 1024);
       const uint64_t do_mn = sdesc_sw128(base + C::kOffDO, kSub, 1024);
       const uint64_t ds_mn = sdesc_sw128(base + C::kOffDS, kSub, 1024);
-      // D-step products of 128-row tiles along d: 16 elements = 32 bytes in
-      // a 128-byte row, 64-column blocks kSub apart
+      // d-step products of 128-row tiles: 16 elements = 32 bytes in a
+      // 128-byte row, 64-column blocks kSub apart
       auto issue_t = [&](uint32_t d_tmem, uint64_t a, uint64_t bd) {
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
@@ -232,113 +314,127 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma_ss(d_tmem, a + off, bd + off, kIdT, ks > 0 ? 1u : 0u);
         }
       };
-      // products over the 128 queries (or keys) of a tile: A from TMEM
-      // (16 bf16 = 8 columns per step), B MN-major (16 rows of 128 bytes)
-      auto issue_g = [&](uint32_t d_tmem, uint32_t a_tmem, uint64_t bd, uint32_t accumulate) {
-#pragma unroll
-        for (int ks = 0; ks < kTile / 16; ++ks)
-          umma_ts(d_tmem, a_tmem + ks * 8, bd + static_cast<uint64_t>((ks * 16 * 128) >> 4),
-                  kIdG, ks > 0 ? 1u : accumulate);
+      // products over queries ks0*16 .. ks1*16-1: A from TMEM (16 bf16 = 8
+      // columns per step), B MN-major (16 rows of 128 bytes per step)
+      auto issue_g = [&](uint32_t d_tmem, uint32_t a_tmem, uint64_t bd, int ks0, int ks1,
+                         bool first) {
+        for (int ks = ks0; ks < ks1; ++ks)
+          umma_ts(d_tmem, a_tmem + ks * 8, bd + static_cast<uint64_t>((ks * 16 * 128) >> 4), kIdG,
+                  (first && ks == 0) ? 0u : 1u);
       };
-      bool ok = mbar_wait(bar(C::bKV), 0, ctl);
-      for (int j = 0; ok && j < n_qt; ++j) {
-        const int st = j % C::NST;
-        const uint32_t ph = (j / C::NST) & 1;
-        const uint32_t par = j & 1;
-        const uint64_t soff = static_cast<uint64_t>((st * C::kTileBytes) >> 4);
-        if (!(ok = mbar_wait(bar(C::bFull(st)), ph, ctl))) break;
-        // S^T reuses the columns of the previous dQ tile once it was read
-        if (j > 0 && !(ok = mbar_wait(bar(C::bDQR), par ^ 1u, ctl))) break;
+      auto stage_off = [](int j) {
+        return static_cast<uint64_t>(((j % C::NST) * C::kTileBytes) >> 4);
+      };
+      bool ok = mbar_wait(bar(C::bKV), 0, ctl) && mbar_wait(bar(C::bFull(0)), 0, ctl);
+      if (ok) {
         tc_fence_after();
-        issue_t(tmem + C::tS, k_desc, q_desc + soff);
+        issue_t(tmem + C::tS, k_desc, q_desc);
         umma_commit(bar(C::bS));
-        issue_t(tmem + C::tDP, v_desc, do_desc + soff);
+        issue_t(tmem + C::tDP, v_desc, do_desc);
         umma_commit(bar(C::bDP));
-        if (!(ok = mbar_wait(bar(C::bP), par, ctl))) break;
+      }
+      for (int j = 0; ok && j < n_qt; ++j) {
+        const uint32_t par = j & 1;
+        const uint64_t soff = stage_off(j);
+        const bool more = j + 1 < n_qt;
+        // dV += P^T dO, each half as soon as the softmax threads stored it
+        if (!(ok = mbar_wait(bar(C::bP0), par, ctl))) break;
         tc_fence_after();
-        issue_g(tmem + C::tDV, tmem + C::tS, do_mn + soff, j > 0 ? 1u : 0u);
+        issue_g(tmem + C::tDV, tmem + C::tS, do_mn + soff, 0, 4, j == 0);
+        if (!(ok = mbar_wait(bar(C::bP1), par, ctl))) break;
+        tc_fence_after();
+        issue_g(tmem + C::tDV, tmem + C::tS, do_mn + soff, 4, 8, j == 0);
+        // S^T of the next tile over the S columns: P^T was read by the
+        // products just issued (MMAs run in issue order)
+        if (more) {
+          const int j1 = j + 1;
+          if (!(ok = mbar_wait(bar(C::bFull(j1 % C::NST)), (j1 / C::NST) & 1, ctl))) break;
+          tc_fence_after();
+          issue_t(tmem + C::tS, k_desc, q_desc + stage_off(j1));
+          umma_commit(bar(C::bS));
+        }
         if (!(ok = mbar_wait(bar(C::bDS), par, ctl))) break;
         tc_fence_after();
-        issue_g(tmem + C::tDK, tmem + C::tDP, q_mn + soff, j > 0 ? 1u : 0u);
-        // dQ tile = dS K: both operands MN-major in shared memory, 16 keys
-        // (16 rows of 128 bytes) per step; it overwrites P^T, which the dV
-        // product above has read (MMAs execute in issue order)
+        issue_g(tmem + C::tDK, tmem + C::tDP, q_mn + soff, 0, 8, j == 0);
+        // dQ^T = K^T dS^T over the 128 keys, 16 per step
+        if (!C::kDqOverDp && j > 0) {
+          if (!(ok = mbar_wait(bar(C::bDQF), par ^ 1u, ctl))) break;
+          tc_fence_after();
+        }
 #pragma unroll
         for (int ks = 0; ks < kTile / 16; ++ks) {
           const uint64_t off = static_cast<uint64_t>((ks * 16 * 128) >> 4);
-          umma_ss(tmem + C::tS, ds_mn + off, k_mn + off, kIdQ, ks > 0 ? 1u : 0u);
+          umma_ss(tmem + C::tDQ, kt_mn + off, ds_mn + off, kIdQ, ks > 0 ? 1u : 0u);
         }
         umma_commit(bar(C::bDQ));
-        umma_commit(bar(C::bEmpty(st)));
+        umma_commit(bar(C::bEmpty(j % C::NST)));
+        if (more) {
+          // d = 128: dQ^T sits over dP^T until it has been read out
+          if (C::kDqOverDp) {
+            if (!(ok = mbar_wait(bar(C::bDQF), par, ctl))) break;
+            tc_fence_after();
+          }
+          issue_t(tmem + C::tDP, v_desc, do_desc + stage_off(j + 1));
+          umma_commit(bar(C::bDP));
+        }
       }
       umma_commit(bar(C::bFinal));
       umma_commit(bar(C::bDrain));
       wait_drain(bar(C::bDrain), 0, p.limit_ns);
     }
-  } else {
-    // ------------------------------------------------------ compute warps
-    const int L = warp * 32 + lane;  // TMEM lane: key k0 + L, or query q0 + L
-    const uint32_t lane_bits = static_cast<uint32_t>(warp * 32) << 16;
-    const uint32_t tl = tmem + lane_bits;
+  } else if (warp < kDqWarp0) {
+    // ------------------------------------------- P and dS (lane = a key)
+    const int L = warp * 32 + lane;
+    const uint32_t tl = tmem + (static_cast<uint32_t>(warp * 32) << 16);
     const int key = k0 + L;
     const bool key_live = key < len;
     const float sl2 = p.scale_log2;
-    const float* lse_h = p.lse + static_cast<size_t>(bh) * p.Lq;
-    const float* dsum_h = p.dsum + static_cast<size_t>(bh) * p.Lq;
     uint8_t* ds_s = gbase + C::kOffDS;
-    // 4 consecutive row values as one float4 only when every row of the head
-    // starts 16-byte aligned (Lq % 4 == 0; the base is 16-byte aligned);
-    // past Lq the value is `fill`
-    const bool vec4 = (p.Lq & 3) == 0;
-    auto load4 = [&](const float* row, int q, float fill) -> float4 {
-      if (vec4 && q + 3 < p.Lq) return __ldg(reinterpret_cast<const float4*>(row + q));
-      return make_float4(q < p.Lq ? __ldg(row + q) : fill, q + 1 < p.Lq ? __ldg(row + q + 1) : fill,
-                         q + 2 < p.Lq ? __ldg(row + q + 2) : fill,
-                         q + 3 < p.Lq ? __ldg(row + q + 3) : fill);
-    };
     bool ok = true;
     for (int j = 0; j < n_qt; ++j) {
+      const int st = j % C::NST;
       const uint32_t par = j & 1;
       const int q0 = (qt_begin + j) * kTile;
-      // ---- P^T row of this key over the tile's 128 queries
+      const float* rows = reinterpret_cast<const float*>(gbase + C::kOffRow + st * 1024);
       if (!(ok = mbar_wait_warp(bar(C::bS), par, ctl))) break;
+      if (!(ok = mbar_wait_warp(bar(C::bFull(st)), (j / C::NST) & 1, ctl))) break;
       tc_fence_after();
-      float pr[kTile];
-      {
-        uint32_t s[kTile];
-        tmem_ld32(tl + C::tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
-        tmem_ld32(tl + C::tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
-        tmem_ld32(tl + C::tS + 64, *reinterpret_cast<uint32_t(*)[32]>(&s[64]));
-        tmem_ld32(tl + C::tS + 96, *reinterpret_cast<uint32_t(*)[32]>(&s[96]));
+      // ---- P^T row of this key, 64 queries at a time, kept as bf16 pairs
+      uint32_t pk[kTile / 2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t s[64];
+        tmem_ld32(tl + C::tS + h * 64, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
+        tmem_ld32(tl + C::tS + h * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
         tmem_ld_wait(s);
 #pragma unroll
-        for (int c = 0; c < kTile; c += 4) {
-          const int q = q0 + c;
-          // lse = +inf for queries past Lq (and rows with no visible key)
-          const float4 lv = load4(lse_h, q, INFINITY);
+        for (int c = 0; c < 64; c += 4) {
+          const float4 lv = *reinterpret_cast<const float4*>(rows + h * 64 + c);
           const float lq[4] = {lv.x, lv.y, lv.z, lv.w};
+          float pv[4];
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            const bool vis = key_live && (!causal || key <= q + u);
-            pr[c + u] = vis ? ex2_approx(fmaf(__uint_as_float(s[c + u]), sl2, -lq[u])) : 0.f;
+            const int q = q0 + h * 64 + c + u;
+            const bool vis = key_live && (!causal || key <= q);
+            pv[u] = vis ? ex2_approx(fmaf(__uint_as_float(s[c + u]), sl2, -lq[u])) : 0.f;
           }
+          pk[h * 32 + c / 2] = pack_bf16x2(pv[0], pv[1]);
+          pk[h * 32 + c / 2 + 1] = pack_bf16x2(pv[2], pv[3]);
         }
-        uint32_t pk[kTile / 2];
-#pragma unroll
-        for (int c = 0; c < kTile / 2; ++c) pk[c] = pack_bf16x2(pr[2 * c], pr[2 * c + 1]);
-        tmem_st32(tl + C::tS + 0, *reinterpret_cast<const uint32_t(*)[32]>(&pk[0]));
-        tmem_st32(tl + C::tS + 32, *reinterpret_cast<const uint32_t(*)[32]>(&pk[32]));
+        // queries 64h .. 64h+63 -> packed columns 32h .. 32h+31 (their S^T
+        // values are already in registers)
+        tmem_st32(tl + C::tS + h * 32, *reinterpret_cast<const uint32_t(*)[32]>(&pk[h * 32]));
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar(h == 0 ? C::bP0 : C::bP1));
       }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(bar(C::bP));
       // ---- dS^T = P^T (dP^T - D), 32 queries at a time; bf16 into TMEM
       // over dP^T (columns already read) and into shared memory as the
-      // MN-major A operand of the dQ product (row = key, 64-query blocks)
+      // MN-major B of the dQ product (row = key, 64-query blocks).  The dQ
+      // product of the previous tile, the last reader of that buffer, has
+      // completed: dP^T(j) was committed after it.
       if (!(ok = mbar_wait_warp(bar(C::bDP), par, ctl))) break;
       tc_fence_after();
-      // the dQ product of the previous tile has read dS from shared memory:
-      // its completion (bDQ of j - 1) was awaited before the dQ readback
 #pragma unroll
       for (int cc = 0; cc < kTile / 32; ++cc) {
         uint32_t dp[32];
@@ -347,17 +443,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t dsk[16];
 #pragma unroll
         for (int i = 0; i < 32; i += 4) {
-          const int q = q0 + cc * 32 + i;
-          const float4 dv = load4(dsum_h, q, 0.f);
-          const float ds0 = pr[cc * 32 + i] * (__uint_as_float(dp[i]) - dv.x);
-          const float ds1 = pr[cc * 32 + i + 1] * (__uint_as_float(dp[i + 1]) - dv.y);
-          const float ds2 = pr[cc * 32 + i + 2] * (__uint_as_float(dp[i + 2]) - dv.z);
-          const float ds3 = pr[cc * 32 + i + 3] * (__uint_as_float(dp[i + 3]) - dv.w);
+          const float4 dv = *reinterpret_cast<const float4*>(rows + 128 + cc * 32 + i);
+          const uint32_t p01 = pk[(cc * 32 + i) / 2], p23 = pk[(cc * 32 + i) / 2 + 1];
+          const float ds0 = bf16_lo(p01) * (__uint_as_float(dp[i]) - dv.x);
+          const float ds1 = bf16_hi(p01) * (__uint_as_float(dp[i + 1]) - dv.y);
+          const float ds2 = bf16_lo(p23) * (__uint_as_float(dp[i + 2]) - dv.z);
+          const float ds3 = bf16_hi(p23) * (__uint_as_float(dp[i + 3]) - dv.w);
           dsk[i / 2] = pack_bf16x2(ds0, ds1);
           dsk[i / 2 + 1] = pack_bf16x2(ds2, ds3);
         }
-        // TMEM: 32 queries of bf16 = 16 columns at 128 + 16 cc (inside the
-        // dP^T columns this thread has already loaded)
         asm volatile(
             "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
             "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(
@@ -380,74 +474,50 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bar(C::bDS));
-      // ---- dQ tile (lane = query q0 + L): scale, add into the fp32 dQ
-      if (!(ok = mbar_wait_warp(bar(C::bDQ), par, ctl))) break;
-      tc_fence_after();
-      const int q = q0 + L;
-      float* dq_row = p.dq + (static_cast<size_t>(bh) * p.Lq + q) * D;
-#pragma unroll
-      for (int cb = 0; cb < D / 32; ++cb) {
-        uint32_t g[32];
-        tmem_ld32(tl + C::tS + cb * 32, g);
-        tmem_ld_wait(g);
-        if (q < p.Lq) {
-#pragma unroll
-          for (int i = 0; i < 32; i += 4)
-            red_add_v4(dq_row + cb * 32 + i, __uint_as_float(g[i]) * p.scale,
-                       __uint_as_float(g[i + 1]) * p.scale, __uint_as_float(g[i + 2]) * p.scale,
-                       __uint_as_float(g[i + 3]) * p.scale);
-        }
-      }
-      tc_fence_before();
-      mbar_arrive(bar(C::bDQR));
     }
-    // ---- epilogue: dV and scale dK for this key
+    // ---- epilogue: dV of this key
     bool have = ok && n_qt > 0;
     if (have) {
       have = mbar_wait_warp(bar(C::bFinal), 0, ctl);
       tc_fence_after();
     }
-    // tcgen05.ld is warp-collective: the whole warp loads (have is uniform
-    // across the warp), and only the stores are limited to keys below Lk
-    {
-      const size_t row = (static_cast<size_t>(bh) * p.Lk + key) * D;
+    store_key_grad<D>(tl + C::tDV, have, 1.f, p.dv,
+                      (static_cast<size_t>(bh) * p.Lk + key) * D, key < p.Lk, p.out_f32 != 0);
+  } else {
+    // ---------------------------------------- dQ tile out (lane = a d index)
+    const int quarter = warp & 3;
+    const int t = quarter * 32 + lane;
+    const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    float* dq_h = p.dq + static_cast<size_t>(bh) * p.Lq * D;
+    bool ok = true;
+    for (int j = 0; j < n_qt; ++j) {
+      const int q0 = (qt_begin + j) * kTile;
+      if (!(ok = mbar_wait_warp(bar(C::bDQ), j & 1, ctl))) break;
+      tc_fence_after();
+      uint32_t g[kTile];
 #pragma unroll
-      for (int which = 0; which < 2; ++which) {
-        const uint32_t col = which == 0 ? C::tDV : C::tDK;
-        const float mul = which == 0 ? 1.f : p.scale;
-        void* out = which == 0 ? p.dv : p.dk;
+      for (int cb = 0; cb < kTile / 32; ++cb)
+        tmem_ld32(tl + C::tDQ + cb * 32, *reinterpret_cast<uint32_t(*)[32]>(&g[cb * 32]));
+      tmem_ld_wait(g);
+      tc_fence_before();
+      mbar_arrive(bar(C::bDQF));
+      if (t < D) {
+        const int nq = min(kTile, p.Lq - q0);
+        float* col = dq_h + static_cast<size_t>(q0) * D + t;
 #pragma unroll
-        for (int cb = 0; cb < D / 32; ++cb) {
-          uint32_t g[32];
-          if (have) {
-            tmem_ld32(tl + col + cb * 32, g);
-            tmem_ld_wait(g);
-          } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) g[i] = 0u;
-          }
-          if (key >= p.Lk) continue;
-          if (p.out_f32) {
-            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out) + row + cb * 32);
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-              dst[i] = make_float4(__uint_as_float(g[4 * i]) * mul, __uint_as_float(g[4 * i + 1]) * mul,
-                                   __uint_as_float(g[4 * i + 2]) * mul,
-                                   __uint_as_float(g[4 * i + 3]) * mul);
-          } else {
-            uint4* dst =
-                reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out) + row + cb * 32);
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              dst[i] = make_uint4(
-                  pack_bf16x2(__uint_as_float(g[8 * i]) * mul, __uint_as_float(g[8 * i + 1]) * mul),
-                  pack_bf16x2(__uint_as_float(g[8 * i + 2]) * mul, __uint_as_float(g[8 * i + 3]) * mul),
-                  pack_bf16x2(__uint_as_float(g[8 * i + 4]) * mul, __uint_as_float(g[8 * i + 5]) * mul),
-                  pack_bf16x2(__uint_as_float(g[8 * i + 6]) * mul, __uint_as_float(g[8 * i + 7]) * mul));
-          }
-        }
+        for (int q = 0; q < kTile; ++q)
+          if (q < nq) red_add_f32(col + q * D, __uint_as_float(g[q]) * p.scale);
       }
     }
+    // ---- epilogue: scale dK of the key on this TMEM lane
+    bool have = ok && n_qt > 0;
+    if (have) {
+      have = mbar_wait_warp(bar(C::bFinal), 0, ctl);
+      tc_fence_after();
+    }
+    const int key = k0 + t;
+    store_key_grad<D>(tl + C::tDK, have, p.scale, p.dk,
+                      (static_cast<size_t>(bh) * p.Lk + key) * D, key < p.Lk, p.out_f32 != 0);
   }
 
   tc_fence_before();
