@@ -18,8 +18,8 @@
 // Keys sit on the MMA's M side (TMEM lanes):
 //   S^T  = K Q^T        M 128 keys, N 128 queries, K = d      TMEM cols 0-127
 //   dP^T = V dO^T       same shape                            TMEM cols 128-255
-//   P^T  -> bf16 over S^T's first 64 columns, in two halves of 64 queries
-//   dS^T -> bf16 over dP^T's first 64 columns, and into shared memory
+//   P^T  -> bf16 pairs: queries 0-63 in S^T cols 0-31, 64-127 in cols 64-95
+//   dS^T -> bf16 pairs in the same places of dP^T, and into shared memory
 //   dV  += P^T dO       A = P^T from TMEM, B = dO (MN-major)  TMEM dV
 //   dK  += dS^T Q       A = dS^T from TMEM, B = Q (MN-major)  TMEM dK
 //   dQ^T = K^T dS^T     A = K (MN-major), B = dS^T (MN-major, the shared
@@ -30,12 +30,15 @@
 // warp's lanes hold 32 consecutive d of one query row, so each reduction
 // instruction covers 128 contiguous bytes.
 //
-// Warps 0-3 compute P and dS (one key per TMEM lane), warps 4-7 move the dQ
-// tile out (one d per lane) and write dK at the end, warp 8 loads (TMA, and
-// the tile's lse and D rows into shared memory), warp 9 issues the MMAs in
-// the order dV(j), S^T(j+1), dK(j), dQ^T(j), dP^T(j+1), so the next tile's
-// exponentials run under this tile's dK and dQ products.  Every wait is
-// bounded.
+// Warps 0-7 compute P and dS: warp w takes the keys on TMEM lanes
+// 32 (w % 4) .. +31 and the 64 queries of half w / 4, two such warps per
+// SM sub-partition.  Each half writes P and dS only inside the columns it
+// alone reads.  Warps 8-11 move the dQ tile out (one d per lane) and write
+// dK at the end, warp 12 loads (TMA, and the tile's -lse and -D rows into
+// shared memory), warp 13 issues the MMAs in the order dV(j), S^T(j+1),
+// dK(j), dQ^T(j), dP^T(j+1), so the next tile's exponentials run under this
+// tile's dK and dQ products.  Every wait is bounded; waiting threads sleep
+// on the barrier instead of spinning.
 #include <math.h>
 #include <stdint.h>
 
@@ -50,10 +53,10 @@ namespace {
 
 constexpr int kTile = 128;       // keys per CTA = queries per step
 constexpr int kSub = 16384;      // one 128-row x 64-column bf16 box
-constexpr int kThreads = 320;
-constexpr int kDqWarp0 = 4;      // warps 4-7
-constexpr int kLoadWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kPdsWarps = 8;     // warps 0-7; warps 8-11 move dQ out
+constexpr int kLoadWarp = 12;
+constexpr int kMmaWarp = 13;
+constexpr int kThreads = 32 * (kMmaWarp + 1);
 constexpr uint32_t kTmemCols = 512;
 constexpr int kMaxSmem = 232448;  // per-CTA opt-in limit
 
@@ -69,7 +72,7 @@ struct BwdCfg {
   static constexpr int kOffQ = kOffV + kTileBytes;                 // NST stages
   static constexpr int kOffDO = kOffQ + NST * kTileBytes;          // NST stages
   static constexpr int kOffDS = kOffDO + NST * kTileBytes;         // dS, 2 x 64 queries
-  static constexpr int kOffRow = kOffDS + 2 * kSub;                // NST x {lse[128], D[128]}
+  static constexpr int kOffRow = kOffDS + 2 * kSub;                // NST x {-lse[128], -D[128]}
   static constexpr int kOffBar = kOffRow + NST * 1024;
   // barriers
   static constexpr int bKV = 0;
@@ -122,28 +125,81 @@ __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, uint64
   }
 }
 
+// try_wait with a suspend-time hint: a thread whose phase is not complete
+// sleeps on the barrier (up to 20 us) instead of re-polling.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity), "r"(20000u)
+      : "memory");
+  return done != 0;
+}
+
+// Bounded wait that sleeps between polls: false when the CTA is aborting or
+// the wait ran past its limit (then the abort flag and the timeout bit are
+// set), as mbar_wait.
+__device__ __forceinline__ bool mbar_wait_s(uint32_t bar, uint32_t parity, const WaitCtl& ctl) {
+  if (mbar_try_wait_sleep(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (;;) {
+    if (mbar_try_wait_sleep(bar, parity)) return true;
+    if (*ctl.abort_flag) return false;
+    if (global_timer_ns() - t0 > ctl.limit_ns) {
+      *ctl.abort_flag = 1;
+      atomicOr(ctl.err, kErrTimeout);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ bool mbar_wait_s_warp(uint32_t bar, uint32_t parity,
+                                                 const WaitCtl& ctl) {
+  const bool ok = mbar_wait_s(bar, parity, ctl);
+  return __all_sync(0xffffffffu, ok);
+}
+
 __device__ __forceinline__ void red_add_f32(float* addr, float v) {
   asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
 }
 
-// 4 consecutive values of a per-row array from row q on; `fill` past Lq.
-// One float4 only when every head's row starts 16-byte aligned (Lq % 4 == 0).
-__device__ __forceinline__ float4 load_row4(const float* row, int q, int Lq, float fill) {
-  if ((Lq & 3) == 0 && q + 3 < Lq) return __ldg(reinterpret_cast<const float4*>(row + q));
-  return make_float4(q < Lq ? __ldg(row + q) : fill, q + 1 < Lq ? __ldg(row + q + 1) : fill,
-                     q + 2 < Lq ? __ldg(row + q + 2) : fill, q + 3 < Lq ? __ldg(row + q + 3) : fill);
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;"
+      : "=l"(d)
+      : "l"(*reinterpret_cast<uint64_t*>(&a)), "l"(*reinterpret_cast<uint64_t*>(&b)));
+  return *reinterpret_cast<float2*>(&d);
 }
 
-__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
+// 4 consecutive values of a per-row array from row q on, negated; `fill`
+// past Lq.  One float4 only when every head's row starts 16-byte aligned
+// (Lq % 4 == 0).
+__device__ __forceinline__ float4 load_row4_neg(const float* row, int q, int Lq, float fill) {
+  float4 v;
+  if ((Lq & 3) == 0 && q + 3 < Lq) {
+    v = __ldg(reinterpret_cast<const float4*>(row + q));
+    return make_float4(-v.x, -v.y, -v.z, -v.w);
+  }
+  return make_float4(q < Lq ? -__ldg(row + q) : fill, q + 1 < Lq ? -__ldg(row + q + 1) : fill,
+                     q + 2 < Lq ? -__ldg(row + q + 2) : fill,
+                     q + 3 < Lq ? -__ldg(row + q + 3) : fill);
+}
 
-// dK or dV of this thread's key from TMEM (whole warp; zeros when `have` is
-// false), times `mul`, stored for key < Lk.
-template <int D>
+__device__ __forceinline__ float2 unpack_bf16x2(uint32_t v) {
+  return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));
+}
+
+// NCB x 32 columns of dK or dV of this thread's key from TMEM (whole warp;
+// zeros when `have` is false), times `mul`, stored from column `c0` for a
+// key below Lk.
+template <int NCB>
 __device__ __forceinline__ void store_key_grad(uint32_t taddr, bool have, float mul, void* out,
                                                size_t row, bool live, bool f32) {
 #pragma unroll
-  for (int cb = 0; cb < D / 32; ++cb) {
+  for (int cb = 0; cb < NCB; ++cb) {
     uint32_t g[32];
     if (have) {
       tmem_ld32(taddr + cb * 32, g);
@@ -173,8 +229,10 @@ __device__ __forceinline__ void store_key_grad(uint32_t taddr, bool have, float 
   }
 }
 
+// 14 warps: two SM sub-partitions hold four of them, and a sub-partition has
+// 16K registers, so 128 per thread at most
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __maxnreg__(128)
     sdpa_bwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ,
                          const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV,
@@ -206,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(C::bDP), 1);
     mbar_init(bar(C::bP0), 128);
     mbar_init(bar(C::bP1), 128);
-    mbar_init(bar(C::bDS), 128);
+    mbar_init(bar(C::bDS), 32 * kPdsWarps);
     mbar_init(bar(C::bDQ), 1);
     mbar_init(bar(C::bDQF), 128);
     mbar_init(bar(C::bFinal), 1);
@@ -265,12 +323,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < n_qt; ++j) {
         const int st = j % C::NST;
         const uint32_t ph = (j / C::NST) & 1;
-        if (!mbar_wait_warp(bar(C::bEmpty(st)), ph ^ 1u, ctl)) break;
+        if (!mbar_wait_s_warp(bar(C::bEmpty(st)), ph ^ 1u, ctl)) break;
         const int q0 = (qt_begin + j) * kTile;
-        // the tile's lse (+inf past Lq, so P = 0 there) and D rows, 4 per lane
+        // the tile's -lse (-inf past Lq, so P = 0 there) and -D rows, 4 per lane
         float4* rows = reinterpret_cast<float4*>(gbase + C::kOffRow + st * 1024);
-        rows[lane] = load_row4(lse_h, q0 + 4 * lane, p.Lq, INFINITY);
-        rows[32 + lane] = load_row4(dsum_h, q0 + 4 * lane, p.Lq, 0.f);
+        rows[lane] = load_row4_neg(lse_h, q0 + 4 * lane, p.Lq, -INFINITY);
+        rows[32 + lane] = load_row4_neg(dsum_h, q0 + 4 * lane, p.Lq, 0.f);
         __syncwarp();  // the lanes' stores precede lane 0's arrive (a release)
         if (lane == 0) {
           mbar_expect_tx(bar(C::bFull(st)), 2 * C::kTileBytes);
@@ -314,18 +372,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma_ss(d_tmem, a + off, bd + off, kIdT, ks > 0 ? 1u : 0u);
         }
       };
-      // products over queries ks0*16 .. ks1*16-1: A from TMEM (16 bf16 = 8
-      // columns per step), B MN-major (16 rows of 128 bytes per step)
-      auto issue_g = [&](uint32_t d_tmem, uint32_t a_tmem, uint64_t bd, int ks0, int ks1,
-                         bool first) {
-        for (int ks = ks0; ks < ks1; ++ks)
-          umma_ts(d_tmem, a_tmem + ks * 8, bd + static_cast<uint64_t>((ks * 16 * 128) >> 4), kIdG,
-                  (first && ks == 0) ? 0u : 1u);
+      // products over the 64 queries of half h: A = bf16 pairs in TMEM at
+      // columns 64 h + 8 k (16 queries per step), B MN-major (16 rows of 128
+      // bytes per step)
+      auto issue_g = [&](uint32_t d_tmem, uint32_t a_tmem, uint64_t bd, int h, bool first) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          umma_ts(d_tmem, a_tmem + 64 * h + 8 * k,
+                  bd + static_cast<uint64_t>(((64 * h + 16 * k) * 128) >> 4), kIdG,
+                  (first && h == 0 && k == 0) ? 0u : 1u);
       };
       auto stage_off = [](int j) {
         return static_cast<uint64_t>(((j % C::NST) * C::kTileBytes) >> 4);
       };
-      bool ok = mbar_wait(bar(C::bKV), 0, ctl) && mbar_wait(bar(C::bFull(0)), 0, ctl);
+      bool ok = mbar_wait_s(bar(C::bKV), 0, ctl) && mbar_wait_s(bar(C::bFull(0)), 0, ctl);
       if (ok) {
         tc_fence_after();
         issue_t(tmem + C::tS, k_desc, q_desc);
@@ -337,28 +397,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t par = j & 1;
         const uint64_t soff = stage_off(j);
         const bool more = j + 1 < n_qt;
-        // dV += P^T dO, each half as soon as the softmax threads stored it
-        if (!(ok = mbar_wait(bar(C::bP0), par, ctl))) break;
+        // dV += P^T dO, each half as soon as its softmax warps stored it
+        if (!(ok = mbar_wait_s(bar(C::bP0), par, ctl))) break;
         tc_fence_after();
-        issue_g(tmem + C::tDV, tmem + C::tS, do_mn + soff, 0, 4, j == 0);
-        if (!(ok = mbar_wait(bar(C::bP1), par, ctl))) break;
+        issue_g(tmem + C::tDV, tmem + C::tS, do_mn + soff, 0, j == 0);
+        if (!(ok = mbar_wait_s(bar(C::bP1), par, ctl))) break;
         tc_fence_after();
-        issue_g(tmem + C::tDV, tmem + C::tS, do_mn + soff, 4, 8, j == 0);
+        issue_g(tmem + C::tDV, tmem + C::tS, do_mn + soff, 1, j == 0);
         // S^T of the next tile over the S columns: P^T was read by the
         // products just issued (MMAs run in issue order)
         if (more) {
           const int j1 = j + 1;
-          if (!(ok = mbar_wait(bar(C::bFull(j1 % C::NST)), (j1 / C::NST) & 1, ctl))) break;
+          if (!(ok = mbar_wait_s(bar(C::bFull(j1 % C::NST)), (j1 / C::NST) & 1, ctl))) break;
           tc_fence_after();
           issue_t(tmem + C::tS, k_desc, q_desc + stage_off(j1));
           umma_commit(bar(C::bS));
         }
-        if (!(ok = mbar_wait(bar(C::bDS), par, ctl))) break;
+        if (!(ok = mbar_wait_s(bar(C::bDS), par, ctl))) break;
         tc_fence_after();
-        issue_g(tmem + C::tDK, tmem + C::tDP, q_mn + soff, 0, 8, j == 0);
+        issue_g(tmem + C::tDK, tmem + C::tDP, q_mn + soff, 0, j == 0);
+        issue_g(tmem + C::tDK, tmem + C::tDP, q_mn + soff, 1, j == 0);
         // dQ^T = K^T dS^T over the 128 keys, 16 per step
         if (!C::kDqOverDp && j > 0) {
-          if (!(ok = mbar_wait(bar(C::bDQF), par ^ 1u, ctl))) break;
+          if (!(ok = mbar_wait_s(bar(C::bDQF), par ^ 1u, ctl))) break;
           tc_fence_after();
         }
 #pragma unroll
@@ -371,7 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (more) {
           // d = 128: dQ^T sits over dP^T until it has been read out
           if (C::kDqOverDp) {
-            if (!(ok = mbar_wait(bar(C::bDQF), par, ctl))) break;
+            if (!(ok = mbar_wait_s(bar(C::bDQF), par, ctl))) break;
             tc_fence_after();
           }
           issue_t(tmem + C::tDP, v_desc, do_desc + stage_off(j + 1));
@@ -382,91 +443,114 @@ __global__ void __launch_bounds__(kThreads, 1)
       umma_commit(bar(C::bDrain));
       wait_drain(bar(C::bDrain), 0, p.limit_ns);
     }
-  } else if (warp < kDqWarp0) {
-    // ------------------------------------------- P and dS (lane = a key)
-    const int L = warp * 32 + lane;
-    const uint32_t tl = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+  } else if (warp < kPdsWarps) {
+    // ------------------------- P and dS (lane = a key, half = 64 queries)
+    const int quarter = warp & 3;
+    const int half = warp >> 2;
+    const int L = quarter * 32 + lane;
+    const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const int key = k0 + L;
     const bool key_live = key < len;
-    const float sl2 = p.scale_log2;
-    uint8_t* ds_s = gbase + C::kOffDS;
+    const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
+    uint8_t* ds_row = gbase + C::kOffDS + half * kSub + (L >> 3) * 1024 + (L & 7) * 128;
     bool ok = true;
     for (int j = 0; j < n_qt; ++j) {
       const int st = j % C::NST;
       const uint32_t par = j & 1;
-      const int q0 = (qt_begin + j) * kTile;
-      const float* rows = reinterpret_cast<const float*>(gbase + C::kOffRow + st * 1024);
-      if (!(ok = mbar_wait_warp(bar(C::bS), par, ctl))) break;
-      if (!(ok = mbar_wait_warp(bar(C::bFull(st)), (j / C::NST) & 1, ctl))) break;
+      const int qh = (qt_begin + j) * kTile + half * 64;   // first query of this half
+      const float* nrow = reinterpret_cast<const float*>(gbase + C::kOffRow + st * 1024);
+      const float* nlse = nrow + half * 64;
+      const float* nd = nrow + 128 + half * 64;
+      if (!(ok = mbar_wait_s_warp(bar(C::bS), par, ctl))) break;
+      if (!(ok = mbar_wait_s_warp(bar(C::bFull(st)), (j / C::NST) & 1, ctl))) break;
       tc_fence_after();
-      // ---- P^T row of this key, 64 queries at a time, kept as bf16 pairs
-      uint32_t pk[kTile / 2];
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
+      // ---- P^T of this key over the half's 64 queries, kept as bf16 pairs
+      uint32_t pk[32];
+      {
         uint32_t s[64];
-        tmem_ld32(tl + C::tS + h * 64, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
-        tmem_ld32(tl + C::tS + h * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
+        tmem_ld32(tl + C::tS + half * 64, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
+        tmem_ld32(tl + C::tS + half * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
         tmem_ld_wait(s);
+        // every query of the half sees this key / none does / some do
+        const bool all_vis = key_live && (!causal || key <= qh);
+        const bool none_vis = !key_live || (causal && key > qh + 63);
+        if (all_vis) {
 #pragma unroll
-        for (int c = 0; c < 64; c += 4) {
-          const float4 lv = *reinterpret_cast<const float4*>(rows + h * 64 + c);
-          const float lq[4] = {lv.x, lv.y, lv.z, lv.w};
-          float pv[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int q = q0 + h * 64 + c + u;
-            const bool vis = key_live && (!causal || key <= q);
-            pv[u] = vis ? ex2_approx(fmaf(__uint_as_float(s[c + u]), sl2, -lq[u])) : 0.f;
+          for (int c = 0; c < 64; c += 4) {
+            const float4 nl = *reinterpret_cast<const float4*>(nlse + c);
+            const float2 x01 = ffma2(make_float2(__uint_as_float(s[c]), __uint_as_float(s[c + 1])),
+                                     sl2, make_float2(nl.x, nl.y));
+            const float2 x23 = ffma2(
+                make_float2(__uint_as_float(s[c + 2]), __uint_as_float(s[c + 3])), sl2,
+                make_float2(nl.z, nl.w));
+            pk[c / 2] = pack_bf16x2(ex2_approx(x01.x), ex2_approx(x01.y));
+            pk[c / 2 + 1] = pack_bf16x2(ex2_approx(x23.x), ex2_approx(x23.y));
           }
-          pk[h * 32 + c / 2] = pack_bf16x2(pv[0], pv[1]);
-          pk[h * 32 + c / 2 + 1] = pack_bf16x2(pv[2], pv[3]);
+        } else if (none_vis) {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) pk[c] = 0u;
+        } else {
+          // the diagonal tile: query q sees this key when key <= q
+          const int first = key - qh;   // first visible column, in (0, 63]
+#pragma unroll
+          for (int c = 0; c < 64; c += 2) {
+            const float2 nl = *reinterpret_cast<const float2*>(nlse + c);
+            const float2 x = ffma2(make_float2(__uint_as_float(s[c]), __uint_as_float(s[c + 1])),
+                                   sl2, nl);
+            pk[c / 2] = pack_bf16x2(c >= first ? ex2_approx(x.x) : 0.f,
+                                    c + 1 >= first ? ex2_approx(x.y) : 0.f);
+          }
         }
-        // queries 64h .. 64h+63 -> packed columns 32h .. 32h+31 (their S^T
-        // values are already in registers)
-        tmem_st32(tl + C::tS + h * 32, *reinterpret_cast<const uint32_t(*)[32]>(&pk[h * 32]));
+        // queries of half h -> bf16 pairs at columns 64 h .. 64 h + 31 (their
+        // S^T values are already in registers; the other half's warps read
+        // only columns 64 (1 - h) ..).  The branches above may split the
+        // warp on the diagonal tile: reconverge before the collective store.
+        __syncwarp();
+        tmem_st32(tl + C::tS + half * 64, pk);
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(bar(h == 0 ? C::bP0 : C::bP1));
+        mbar_arrive(bar(half == 0 ? C::bP0 : C::bP1));
       }
-      // ---- dS^T = P^T (dP^T - D), 32 queries at a time; bf16 into TMEM
-      // over dP^T (columns already read) and into shared memory as the
-      // MN-major B of the dQ product (row = key, 64-query blocks).  The dQ
-      // product of the previous tile, the last reader of that buffer, has
-      // completed: dP^T(j) was committed after it.
-      if (!(ok = mbar_wait_warp(bar(C::bDP), par, ctl))) break;
+      // ---- dS^T = P^T (dP^T - D) over the half, 32 queries at a time; bf16
+      // pairs into TMEM at dP^T columns 64 h .. (already read) and into
+      // shared memory as the MN-major B of the dQ product (row = key,
+      // 64-query blocks).  The dQ product of the previous tile, the last
+      // reader of that buffer, has completed: dP^T(j) was committed after it.
+      if (!(ok = mbar_wait_s_warp(bar(C::bDP), par, ctl))) break;
       tc_fence_after();
 #pragma unroll
-      for (int cc = 0; cc < kTile / 32; ++cc) {
+      for (int cc = 0; cc < 2; ++cc) {
         uint32_t dp[32];
-        tmem_ld32(tl + C::tDP + cc * 32, dp);
+        tmem_ld32(tl + C::tDP + half * 64 + cc * 32, dp);
         tmem_ld_wait(dp);
         uint32_t dsk[16];
 #pragma unroll
         for (int i = 0; i < 32; i += 4) {
-          const float4 dv = *reinterpret_cast<const float4*>(rows + 128 + cc * 32 + i);
-          const uint32_t p01 = pk[(cc * 32 + i) / 2], p23 = pk[(cc * 32 + i) / 2 + 1];
-          const float ds0 = bf16_lo(p01) * (__uint_as_float(dp[i]) - dv.x);
-          const float ds1 = bf16_hi(p01) * (__uint_as_float(dp[i + 1]) - dv.y);
-          const float ds2 = bf16_lo(p23) * (__uint_as_float(dp[i + 2]) - dv.z);
-          const float ds3 = bf16_hi(p23) * (__uint_as_float(dp[i + 3]) - dv.w);
-          dsk[i / 2] = pack_bf16x2(ds0, ds1);
-          dsk[i / 2 + 1] = pack_bf16x2(ds2, ds3);
+          const float4 ndv = *reinterpret_cast<const float4*>(nd + cc * 32 + i);
+          const float2 d01 = fadd2(make_float2(__uint_as_float(dp[i]), __uint_as_float(dp[i + 1])),
+                                   make_float2(ndv.x, ndv.y));
+          const float2 d23 = fadd2(
+              make_float2(__uint_as_float(dp[i + 2]), __uint_as_float(dp[i + 3])),
+              make_float2(ndv.z, ndv.w));
+          const float2 s01 = fmul2(unpack_bf16x2(pk[cc * 16 + i / 2]), d01);
+          const float2 s23 = fmul2(unpack_bf16x2(pk[cc * 16 + i / 2 + 1]), d23);
+          dsk[i / 2] = pack_bf16x2(s01.x, s01.y);
+          dsk[i / 2 + 1] = pack_bf16x2(s23.x, s23.y);
         }
         asm volatile(
             "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
             "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(
-                tl + C::tDP + cc * 16),
+                tl + C::tDP + half * 64 + cc * 16),
             "r"(dsk[0]), "r"(dsk[1]), "r"(dsk[2]), "r"(dsk[3]), "r"(dsk[4]), "r"(dsk[5]),
             "r"(dsk[6]), "r"(dsk[7]), "r"(dsk[8]), "r"(dsk[9]), "r"(dsk[10]), "r"(dsk[11]),
             "r"(dsk[12]), "r"(dsk[13]), "r"(dsk[14]), "r"(dsk[15])
             : "memory");
-        // shared memory: queries [32 cc, 32 cc + 32) of row L, in block
-        // (32 cc) / 64, 16-byte chunks ((q % 64) / 8) ^ (L % 8)
-        uint8_t* row = ds_s + ((cc * 32) / 64) * kSub + (L >> 3) * 1024 + (L & 7) * 128;
+        // shared memory: queries [32 cc, 32 cc + 32) of the half in row L,
+        // 16-byte chunks (q % 64) / 8, swizzled by L % 8
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const int chunk = (((cc * 32) & 63) >> 3) + u;
-          *reinterpret_cast<uint4*>(row + ((chunk ^ (L & 7)) << 4)) =
+          const int chunk = cc * 4 + u;
+          *reinterpret_cast<uint4*>(ds_row + ((chunk ^ (L & 7)) << 4)) =
               make_uint4(dsk[4 * u], dsk[4 * u + 1], dsk[4 * u + 2], dsk[4 * u + 3]);
         }
       }
@@ -475,14 +559,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(bar(C::bDS));
     }
-    // ---- epilogue: dV of this key
+    // ---- epilogue: half h writes dV columns [h d/2, (h + 1) d/2) of its key
     bool have = ok && n_qt > 0;
     if (have) {
-      have = mbar_wait_warp(bar(C::bFinal), 0, ctl);
+      have = mbar_wait_s_warp(bar(C::bFinal), 0, ctl);
       tc_fence_after();
     }
-    store_key_grad<D>(tl + C::tDV, have, 1.f, p.dv,
-                      (static_cast<size_t>(bh) * p.Lk + key) * D, key < p.Lk, p.out_f32 != 0);
+    store_key_grad<D / 64>(tl + C::tDV + half * (D / 2), have, 1.f, p.dv,
+                           (static_cast<size_t>(bh) * p.Lk + key) * D + half * (D / 2),
+                           key < p.Lk, p.out_f32 != 0);
   } else {
     // ---------------------------------------- dQ tile out (lane = a d index)
     const int quarter = warp & 3;
@@ -492,7 +577,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int j = 0; j < n_qt; ++j) {
       const int q0 = (qt_begin + j) * kTile;
-      if (!(ok = mbar_wait_warp(bar(C::bDQ), j & 1, ctl))) break;
+      if (!(ok = mbar_wait_s_warp(bar(C::bDQ), j & 1, ctl))) break;
       tc_fence_after();
       uint32_t g[kTile];
 #pragma unroll
@@ -512,12 +597,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---- epilogue: scale dK of the key on this TMEM lane
     bool have = ok && n_qt > 0;
     if (have) {
-      have = mbar_wait_warp(bar(C::bFinal), 0, ctl);
+      have = mbar_wait_s_warp(bar(C::bFinal), 0, ctl);
       tc_fence_after();
     }
     const int key = k0 + t;
-    store_key_grad<D>(tl + C::tDK, have, p.scale, p.dk,
-                      (static_cast<size_t>(bh) * p.Lk + key) * D, key < p.Lk, p.out_f32 != 0);
+    store_key_grad<D / 32>(tl + C::tDK, have, p.scale, p.dk,
+                           (static_cast<size_t>(bh) * p.Lk + key) * D, key < p.Lk,
+                           p.out_f32 != 0);
   }
 
   tc_fence_before();
