@@ -188,13 +188,16 @@ size_t sdpa_backward_workspace_bytes(int B, int H, int Lq);
  *   dQ = scale * dS K,  dK = scale * dS^T Q.
  *   Q, O, dO [B, H, Lq, d] bf16; K, V [B, H, Lk, d] bf16 (as in the forward).
  *   lse     : fp32 [B, H, Lq] from sdpa_forward_lse on the same inputs.
- *   dQ      : fp32 [B, H, Lq, d] (written: zeroed, then accumulated).
+ *   dQ      : fp32 [B, H, Lq, d], written once (its sum over keys stays on
+ *             the chip; nothing is accumulated in global memory).
  *   dK, dV  : [B, H, Lk, d] of grad_dtype (MHA_BF16 or MHA_F32).
  *   scale, mask_kind, key_lengths : as in the forward (CAUSAL and
  *             KEY_PADDING; no float mask).
  *   workspace : device, >= sdpa_backward_workspace_bytes(B, H, Lq) bytes.
  * d must be 64 or 128; all pointers 16-byte aligned.  Blocked keys receive
- * zero gradient.  The call allocates nothing.
+ * zero gradient; a query row with no visible key gets dQ = 0.  The call
+ * allocates nothing.  Two kernels run on `stream`: dK and dV (a CTA per key
+ * tile) and dQ (a CTA per query tile), after the row dot products D.
  * Returns MHA_OK, MHA_ERR_INVALID_ARG, MHA_ERR_UNSUPPORTED or MHA_ERR_CUDA.
  */
 mha_status sdpa_backward(const void *Q, const void *K, const void *V,
