@@ -9,7 +9,9 @@ query/key pair, 2*B*H*d*L*(L+1) for causal), summed over all ranks.
 
 Extra legs in the same JSON line:
   e2e          the same metric through the public call with host (pinned)
-               buffers: H2D of Q/K/V and D2H of O inside the timed region
+               buffers (sdpa_forward_host, which overlaps the copies with the
+               attention chunk by chunk): H2D of Q/K/V and D2H of O inside the
+               timed region
   roofline     the fused kernel against the measured bf16 tensor peak
   mha_layer    the whole layer (rows a1-a8: projections with head-split
                stores, attention with the concat store, output projection)

@@ -98,6 +98,38 @@ mha_status sdpa_forward(const void *Q, const void *K, const void *V, void *O,
                         mha_stream stream);
 
 /*
+ * sdpa_forward_host -- sdpa_forward on host buffers: Q, K, V (and the key
+ * lengths) are copied in, attended and O is copied out, in about sixteen
+ * chunks of (b, h) heads whose copies overlap the attention of other chunks
+ * (every head is independent: "How Transformers Work" (worksonmygpu.com),
+ * "Multi-head attention").
+ *   Qh, Kh, Vh, Oh : host, same shapes and types as sdpa_forward; pinned
+ *             (page-locked) memory lets the copies run asynchronously.
+ *   key_lengths_h : host int32[B] or NULL, as sdpa_forward's key_lengths.
+ *   workspace : device, 256-byte aligned, at least
+ *             sdpa_forward_host_workspace_bytes(...) bytes; the call keeps
+ *             device copies of Q, K, V, O and the lengths there.
+ *   stream    : the call is ordered after work already queued on `stream`,
+ *             and `stream` covers it: Oh is complete once `stream` has been
+ *             synchronised.  Two internal copy streams and a second compute
+ *             stream carry the overlap.
+ * Same dtypes, head sizes and checks as sdpa_forward.  The call allocates
+ * nothing on the device; it creates its internal streams and events once per
+ * device.  Calls on one device are serialised on the host while they
+ * enqueue.
+ * Returns MHA_OK, MHA_ERR_INVALID_ARG, MHA_ERR_UNSUPPORTED or MHA_ERR_CUDA.
+ */
+mha_status sdpa_forward_host(const void *Qh, const void *Kh, const void *Vh, void *Oh,
+                             int B, int H, int Lq, int Lk, int d, float scale,
+                             int mask_kind, const int32_t *key_lengths_h,
+                             mha_dtype in_dtype, mha_dtype out_dtype,
+                             void *workspace, size_t workspace_bytes, mha_stream stream);
+
+/* Device workspace sdpa_forward_host needs, in bytes (0 for bad arguments). */
+size_t sdpa_forward_host_workspace_bytes(int B, int H, int Lq, int Lk, int d,
+                                         mha_dtype in_dtype, mha_dtype out_dtype);
+
+/*
  * sdpa_forward_float_mask -- sdpa_forward with an additive float mask added
  * to the scaled scores, the optional mask of the reference SDPA that "The
  * Transformer" (rayaq.ca) describes in "Attention, by hand" (with -inf

@@ -68,6 +68,11 @@ def _declare(lib):
     lib.sdpa_backward.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
                                   f32, i32, vp, i32, vp, ctypes.c_size_t, vp]
     lib.sdpa_backward.restype = i32
+    lib.sdpa_forward_host_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32, i32]
+    lib.sdpa_forward_host_workspace_bytes.restype = ctypes.c_size_t
+    lib.sdpa_forward_host.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, i32, vp, i32,
+                                      i32, vp, ctypes.c_size_t, vp]
+    lib.sdpa_forward_host.restype = i32
     lib.sinusoidal_pe.argtypes = [vp, i32, i32, i32, vp]
     lib.sinusoidal_pe.restype = i32
     lib.embed_pe_forward.argtypes = [vp, vp, i32, vp, i32, vp, i32, i32, i32, i32, f32, i32, vp]
@@ -431,28 +436,31 @@ def set_wait_limit_ms(ms: int) -> int:
 
 
 def sdpa_forward_host(Qh, Kh, Vh, scale=None, mask_kind=MASK_NONE, lengths_h=None,
-                      out_dtype=None, device="cuda", bufs=None):
-    """End-to-end call from host (pinned) tensors: copy in, attend, copy out.
+                      out_dtype=None, device="cuda", bufs=None, stream=None):
+    """End-to-end call from host (pinned) tensors through the library's
+    sdpa_forward_host: copies in, attention and copies out overlap chunk by
+    chunk on the device.  Returns the pinned output; it is complete once
+    ``stream`` (the current stream by default) has been synchronised.
 
-    ``bufs`` (a dict) keeps device and pinned buffers between calls."""
+    ``bufs`` (a dict) keeps the device workspace and the pinned output
+    between calls."""
     bufs = {} if bufs is None else bufs
-
-    def dev(name, src):
-        t = bufs.get(name)
-        if t is None or t.shape != src.shape or t.dtype != src.dtype:
-            t = bufs[name] = torch.empty(src.shape, dtype=src.dtype, device=device)
-        t.copy_(src, non_blocking=True)
-        return t
-
-    Q, K, V = dev("Q", Qh), dev("K", Kh), dev("V", Vh)
-    kl = dev("len", lengths_h) if lengths_h is not None else None
+    B, H, Lq, d = Qh.shape
+    Lk = Kh.shape[2]
     odt = out_dtype or Qh.dtype
-    O = bufs.get("O")
-    if O is None or O.shape != Q.shape or O.dtype != odt:
-        O = bufs["O"] = torch.empty(Q.shape, dtype=odt, device=device)
-    sdpa_forward(Q, K, V, scale=scale, mask_kind=mask_kind, key_lengths=kl, out=O)
+    need = int(lib().sdpa_forward_host_workspace_bytes(B, H, Lq, Lk, d, _dtype_code(Qh.dtype),
+                                                       _dtype_code(odt)))
+    ws = bufs.get("ws")
+    if ws is None or ws.numel() < need:
+        ws = bufs["ws"] = torch.empty(max(256, need), dtype=torch.uint8, device=device)
     Oh = bufs.get("Oh")
-    if Oh is None or Oh.shape != O.shape or Oh.dtype != odt:
-        Oh = bufs["Oh"] = torch.empty(O.shape, dtype=odt, pin_memory=True)
-    Oh.copy_(O, non_blocking=True)
+    if Oh is None or Oh.shape != Qh.shape or Oh.dtype != odt:
+        Oh = bufs["Oh"] = torch.empty(Qh.shape, dtype=odt, pin_memory=True)
+    lp = ctypes.c_void_p(lengths_h.data_ptr()) if lengths_h is not None else None
+    st = lib().sdpa_forward_host(ctypes.c_void_p(Qh.data_ptr()), ctypes.c_void_p(Kh.data_ptr()),
+                                 ctypes.c_void_p(Vh.data_ptr()), ctypes.c_void_p(Oh.data_ptr()),
+                                 B, H, Lq, Lk, d, float(scale or 0.0), int(mask_kind), lp,
+                                 _dtype_code(Qh.dtype), _dtype_code(odt), _dev_ptr(ws),
+                                 ws.numel(), _stream(stream))
+    _check(st, "sdpa_forward_host")
     return Oh
