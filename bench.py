@@ -373,7 +373,7 @@ def bench_sdpa(args, w, rank, world, local_rank):
         mha.sdpa_forward_host(Qh, Kh, Vh, mask_kind=w.mask, lengths_h=lens_h, bufs=bufs)
     torch.cuda.synchronize()
     barrier()
-    e2e_steps = max(2, min(args.steps, 5))
+    e2e_steps = max(3, min(args.steps, 10))
     t0 = time.perf_counter()
     for _ in range(e2e_steps):
         Oh = mha.sdpa_forward_host(Qh, Kh, Vh, mask_kind=w.mask, lengths_h=lens_h, bufs=bufs)

@@ -105,7 +105,10 @@ __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, uint64
 }
 
 template <int D, int NQT, int NST, bool kAddMask, bool kLse>
-__global__ void __launch_bounds__(Cfg<D, NQT, NST>::kThreads, 1)
+// The d = 64 single-tile, two-stage form is built for two CTAs per SM (80 KB
+// of shared memory, 256 TMEM columns and at most 168 registers each).
+__global__ void __launch_bounds__(Cfg<D, NQT, NST>::kThreads,
+                                  (D == 64 && NQT == 1 && NST == 2) ? 2 : 1)
     sdpa_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ,
                          const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, const SdpaParams p) {
@@ -555,6 +558,10 @@ cudaError_t launch_sdpa_bf16(const SdpaArgs& a, const DeviceCtl& ctl) {
                  : launch_impl<128, 1, 2, false, true>(a, ctl);
     return cudaErrorInvalidValue;
   }
+  // d = 64 with at most 16 key tiles: one query tile per CTA and two CTAs per
+  // SM, so one CTA's pipeline fill and epilogue overlap the other's tiles
+  // (measured faster up to Lk = 2048, slower from 8192 on)
+  if (a.d == 64 && a.Lk <= 2048) return launch_impl<64, 1, 2, false>(a, ctl);
   if (a.d == 64)
     return two ? launch_impl<64, 2, 3, false>(a, ctl) : launch_impl<64, 1, 3, false>(a, ctl);
   if (a.d == 128)
