@@ -14,8 +14,14 @@
 // is loaded as 64 x 64 boxes (64 N-columns of 128 bytes, 64 K-rows).
 // Warp roles: warp 0 TMA producer, warp 1 MMA issuer and TMEM owner,
 // warps 2-5 epilogue (TMEM -> registers -> global, one row per thread).
-// Up to three problems of one shape share a launch (grid.z), which is how
-// the Q, K and V projections of self-attention run as one launch.
+// Up to three problems of one shape share a launch, which is how the Q, K
+// and V projections of self-attention run as one launch.
+//
+// The kernel is persistent: one CTA per SM walks the output tiles (problem,
+// then row tile, then column tile, so the CTAs running at once share W and
+// A tiles in L2).  Two 256-column
+// accumulators in tensor memory alternate, so one tile's epilogue drains
+// while the next tile's MMAs run, and the TMA ring runs on across tiles.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -31,13 +37,14 @@ constexpr int kWBox = 64 * 64 * 2;               // 8 KB: one 64(N) x 64(K) box
 constexpr int kWBytes = kBK * kBN * 2;           // 32 KB
 constexpr int kStageBytes = kABytes + kWBytes;   // 48 KB
 constexpr int kThreads = 192;
-constexpr uint32_t kTmemCols = 256;
-// barriers: full[kStages], empty[kStages], acc_full, drain
+constexpr uint32_t kTmemCols = 512;   // two kBN-column accumulators
+// barriers: full[kStages], empty[kStages], acc_full[2], acc_empty[2], drain
 __host__ __device__ constexpr int bFull(int s) { return s; }
 __host__ __device__ constexpr int bEmpty(int s) { return kStages + s; }
-constexpr int bAcc = 2 * kStages;
-constexpr int bDrain = 2 * kStages + 1;
-constexpr int kNumBars = 2 * kStages + 2;
+__host__ __device__ constexpr int bAccFull(int b) { return 2 * kStages + b; }
+__host__ __device__ constexpr int bAccEmpty(int b) { return 2 * kStages + 2 + b; }
+constexpr int bDrain = 2 * kStages + 4;
+constexpr int kNumBars = 2 * kStages + 5;
 constexpr int kOffBar = kStages * kStageBytes;
 constexpr int kOffMisc = kOffBar + 8 * kNumBars;
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;
@@ -51,6 +58,8 @@ struct GemmParams {
   int L[3];
   int dh[3];
   int M, N, K;
+  int count;          // problems in the launch (1..3)
+  int mt, nt;         // row and column tiles per problem
   unsigned* err;
   uint64_t limit_ns;
 };
@@ -77,16 +86,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const WaitCtl ctl{abort_flag, p.err, p.limit_ns};
-  const int z = blockIdx.z;
-  const CUtensorMap* tA = z == 0 ? &tA0 : (z == 1 ? &tA1 : &tA2);
-  const CUtensorMap* tW = z == 0 ? &tW0 : (z == 1 ? &tW1 : &tW2);
+  auto map_a = [&](int z) { return z == 0 ? &tA0 : (z == 1 ? &tA1 : &tA2); };
+  auto map_w = [&](int z) { return z == 0 ? &tW0 : (z == 1 ? &tW1 : &tW2); };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar(bFull(s)), 1);
       mbar_init(bar(bEmpty(s)), 1);
     }
-    mbar_init(bar(bAcc), 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(bAccFull(b)), 1);
+      mbar_init(bar(bAccEmpty(b)), 128);
+    }
     mbar_init(bar(bDrain), 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -96,57 +107,83 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_relinquish();
   }
   if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(tA);
-    tma_prefetch_desc(tW);
+    for (int z = 0; z < p.count; ++z) {
+      tma_prefetch_desc(map_a(z));
+      tma_prefetch_desc(map_w(z));
+    }
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
 
-  const int n0 = blockIdx.x * kBN;
-  const int m0 = blockIdx.y * kBM;
   const int num_k = (p.K + kBK - 1) / kBK;
+  const int num_tiles = p.mt * p.count * p.nt;
+  // tile t: problem, then row tile, then column tile, so the CTAs running
+  // at once share one problem's W (and a few rows of A) in L2
+  auto decode = [&](int t, int& z, int& m0, int& n0) {
+    const int per_z = p.mt * p.nt;
+    z = t / per_z;
+    const int r = t - z * per_z;
+    const int mi = r / p.nt;
+    n0 = (r - mi * p.nt) * kBN;
+    m0 = mi * kBM;
+  };
 
   if (warp == 0) {
     if (lane == 0) {
-      int issued = 0;
-      for (int kt = 0; kt < num_k; ++kt) {
-        const int st = kt % kStages;
-        const uint32_t ph = (kt / kStages) & 1;
-        if (!mbar_wait(bar(bEmpty(st)), ph ^ 1u, ctl)) break;
-        const uint32_t sa = base + st * kStageBytes;
-        mbar_expect_tx(bar(bFull(st)), kStageBytes);
-        tma_load_2d(sa, tA, bar(bFull(st)), kt * kBK, m0);
+      // one ring of stages across all of this CTA's tiles
+      int g = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+        int z, m0, n0;
+        decode(t, z, m0, n0);
+        const CUtensorMap* tA = map_a(z);
+        const CUtensorMap* tW = map_w(z);
+        for (int kt = 0; kt < num_k; ++kt, ++g) {
+          const int st = g % kStages;
+          const uint32_t ph = (g / kStages) & 1;
+          if (!(ok = mbar_wait(bar(bEmpty(st)), ph ^ 1u, ctl))) break;
+          const uint32_t sa = base + st * kStageBytes;
+          mbar_expect_tx(bar(bFull(st)), kStageBytes);
+          tma_load_2d(sa, tA, bar(bFull(st)), kt * kBK, m0);
 #pragma unroll
-        for (int nb = 0; nb < kBN / 64; ++nb)
-          tma_load_2d(sa + kABytes + nb * kWBox, tW, bar(bFull(st)), n0 + nb * 64, kt * kBK);
-        issued = kt + 1;
+          for (int nb = 0; nb < kBN / 64; ++nb)
+            tma_load_2d(sa + kABytes + nb * kWBox, tW, bar(bFull(st)), n0 + nb * 64, kt * kBK);
+        }
       }
-      for (int kt = max(0, issued - kStages); kt < issued; ++kt)
-        wait_drain(bar(bFull(kt % kStages)), (kt / kStages) & 1, p.limit_ns);
+      for (int q = max(0, g - kStages); q < g; ++q)
+        wait_drain(bar(bFull(q % kStages)), (q / kStages) & 1, p.limit_ns);
     }
   } else if (warp == 1) {
     if (lane == 0) {
       constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, kBN, false, true);
+      int g = 0, i = 0;
       bool ok = true;
-      for (int kt = 0; kt < num_k; ++kt) {
-        const int st = kt % kStages;
-        const uint32_t ph = (kt / kStages) & 1;
-        if (!(ok = mbar_wait(bar(bFull(st)), ph, ctl))) break;
+      for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x, ++i) {
+        // accumulator i % 2, once the epilogue has drained its previous tile
+        const int b = i & 1;
+        const uint32_t acc = tmem + static_cast<uint32_t>(b * kBN);
+        if (!(ok = mbar_wait(bar(bAccEmpty(b)), ((i >> 1) & 1) ^ 1u, ctl))) break;
         tc_fence_after();
-        const uint32_t sa = base + st * kStageBytes;
-        const uint32_t sw = sa + kABytes;
+        for (int kt = 0; kt < num_k; ++kt, ++g) {
+          const int st = g % kStages;
+          const uint32_t ph = (g / kStages) & 1;
+          if (!(ok = mbar_wait(bar(bFull(st)), ph, ctl))) break;
+          tc_fence_after();
+          const uint32_t sa = base + st * kStageBytes;
+          const uint32_t sw = sa + kABytes;
 #pragma unroll
-        for (int ks = 0; ks < kBK / 16; ++ks) {
-          // A: K-major, +32 bytes per 16 k; W: MN-major, +16 rows of 128 bytes
-          umma_ss(tmem, sdesc_sw128(sa + ks * 32, 16, 1024),
-                  sdesc_sw128(sw + ks * 16 * 128, kWBox, 1024), kIdesc,
-                  (kt > 0 || ks > 0) ? 1u : 0u);
+          for (int ks = 0; ks < kBK / 16; ++ks) {
+            // A: K-major, +32 bytes per 16 k; W: MN-major, +16 rows of 128 bytes
+            umma_ss(acc, sdesc_sw128(sa + ks * 32, 16, 1024),
+                    sdesc_sw128(sw + ks * 16 * 128, kWBox, 1024), kIdesc,
+                    (kt > 0 || ks > 0) ? 1u : 0u);
+          }
+          umma_commit(bar(bEmpty(st)));
         }
-        umma_commit(bar(bEmpty(st)));
+        if (ok) umma_commit(bar(bAccFull(b)));
       }
-      if (ok) umma_commit(bar(bAcc));
       umma_commit(bar(bDrain));
       wait_drain(bar(bDrain), 0, p.limit_ns);
     }
@@ -154,54 +191,60 @@ __global__ void __launch_bounds__(kThreads, 1)
     // epilogue: warp w may read TMEM lanes [32*(w%4), 32*(w%4)+32)
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
-    const int m = m0 + row;
-    const bool ok = num_k > 0 && mbar_wait_warp(bar(bAcc), 0, ctl);
-    if (ok) tc_fence_after();
-    const int store = p.store[z];
-    const int L = p.L[z], dh = p.dh[z];
-    const __nv_bfloat16* bias = p.bias[z];
-    const int relu = p.relu[z];
-    __nv_bfloat16* C = static_cast<__nv_bfloat16*>(p.C[z]);
-    const uint32_t tbase = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    for (int cb = 0; cb < kBN / 32; ++cb) {
-      const int n = n0 + cb * 32;
-      if (n >= p.N) break;  // uniform across the warp
-      uint32_t v[32];
-      if (ok) {
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    int i = 0;
+    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++i) {
+      int z, m0, n0;
+      decode(t, z, m0, n0);
+      const int b = i & 1;
+      const bool ok = num_k > 0 && mbar_wait_warp(bar(bAccFull(b)), (i >> 1) & 1, ctl);
+      if (!ok) break;
+      tc_fence_after();
+      const int m = m0 + row;
+      const int store = p.store[z];
+      const int L = p.L[z], dh = p.dh[z];
+      const __nv_bfloat16* bias = p.bias[z];
+      const int relu = p.relu[z];
+      __nv_bfloat16* C = static_cast<__nv_bfloat16*>(p.C[z]);
+      const uint32_t tbase = lane_base + static_cast<uint32_t>(b * kBN);
+      for (int cb = 0; cb < kBN / 32; ++cb) {
+        const int n = n0 + cb * 32;
+        if (n >= p.N) break;  // uniform across the warp
+        uint32_t v[32];
         tmem_ld32(tbase + cb * 32, v);
         tmem_ld_wait(v);
-      } else {
+        if (bias) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = 0u;
-      }
-      if (bias) {
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-          v[i] = __float_as_uint(__uint_as_float(v[i]) + __bfloat162float(bias[n + i]));
-      }
-      if (relu) {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(fmaxf(__uint_as_float(v[i]), 0.f));
-      }
-      if (m < p.M) {
-        size_t off;
-        if (store == static_cast<int>(GemmStore::kHeadSplit)) {
-          const int bb = m / L, l = m - bb * L, hh = n / dh, c = n - hh * dh;
-          off = ((static_cast<size_t>(bb) * (p.N / dh) + hh) * L + l) * dh + c;
-        } else {
-          off = static_cast<size_t>(m) * p.N + n;
+          for (int k = 0; k < 32; ++k)
+            v[k] = __float_as_uint(__uint_as_float(v[k]) + __bfloat162float(bias[n + k]));
         }
-        uint4* dst = reinterpret_cast<uint4*>(C + off);
+        if (relu) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          uint4 w;
-          w.x = pack_bf16x2(__uint_as_float(v[8 * i + 0]), __uint_as_float(v[8 * i + 1]));
-          w.y = pack_bf16x2(__uint_as_float(v[8 * i + 2]), __uint_as_float(v[8 * i + 3]));
-          w.z = pack_bf16x2(__uint_as_float(v[8 * i + 4]), __uint_as_float(v[8 * i + 5]));
-          w.w = pack_bf16x2(__uint_as_float(v[8 * i + 6]), __uint_as_float(v[8 * i + 7]));
-          dst[i] = w;
+          for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(fmaxf(__uint_as_float(v[k]), 0.f));
+        }
+        if (m < p.M) {
+          size_t off;
+          if (store == static_cast<int>(GemmStore::kHeadSplit)) {
+            const int bb = m / L, l = m - bb * L, hh = n / dh, c = n - hh * dh;
+            off = ((static_cast<size_t>(bb) * (p.N / dh) + hh) * L + l) * dh + c;
+          } else {
+            off = static_cast<size_t>(m) * p.N + n;
+          }
+          uint4* dst = reinterpret_cast<uint4*>(C + off);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(v[8 * k + 0]), __uint_as_float(v[8 * k + 1]));
+            w.y = pack_bf16x2(__uint_as_float(v[8 * k + 2]), __uint_as_float(v[8 * k + 3]));
+            w.z = pack_bf16x2(__uint_as_float(v[8 * k + 4]), __uint_as_float(v[8 * k + 5]));
+            w.w = pack_bf16x2(__uint_as_float(v[8 * k + 6]), __uint_as_float(v[8 * k + 7]));
+            dst[k] = w;
+          }
         }
       }
+      // this accumulator may take the tile after next
+      tc_fence_before();
+      mbar_arrive(bar(bAccEmpty(b)));
     }
   }
 
@@ -209,6 +252,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc<kTmemCols>(tmem);
+}
+
+int num_sms() {
+  static int n = 0;
+  if (n <= 0) {
+    int dev = 0, v = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0)
+      n = v;
+    else
+      n = 148;
+  }
+  return n;
 }
 
 }  // namespace
@@ -240,12 +296,18 @@ cudaError_t launch_gemm_bf16(const GemmArgs& g, const DeviceCtl& ctl) {
   p.M = g.M;
   p.N = g.N;
   p.K = g.K;
+  p.count = g.count;
+  p.mt = (g.M + kBM - 1) / kBM;
+  p.nt = (g.N + kBN - 1) / kBN;
   p.err = ctl.err;
   p.limit_ns = ctl.limit_ns;
   cudaError_t e = cudaFuncSetAttribute(gemm_bf16_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
-  const dim3 grid((g.N + kBN - 1) / kBN, (g.M + kBM - 1) / kBM, g.count);
+  // persistent: one CTA per SM (shared memory admits no second), or fewer
+  // when there are fewer tiles
+  const long long tiles = static_cast<long long>(p.mt) * p.nt * g.count;
+  const int grid = static_cast<int>(tiles < num_sms() ? tiles : num_sms());
   gemm_bf16_kernel<<<grid, kThreads, kSmemBytes, g.stream>>>(ta[0], ta[1], ta[2], tw[0], tw[1],
                                                               tw[2], p);
   return cudaGetLastError();
