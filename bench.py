@@ -297,6 +297,16 @@ def workload_from_args(args):
 
 # ------------------------------------------------------------------ GPU arm
 
+def fwd_kernel_name(w):
+    """The forward instantiation sdpa_forward picks for workload w:
+    <head dim, query tiles per CTA, K/V stages, keys per tile>."""
+    if w.d == 128:
+        return f"sdpa_fwd_bf16_kernel<128,{2 if w.Lq > 128 else 1},2,128>"
+    if w.Lq > 128:
+        return "sdpa_fwd_bf16_kernel<64,2,3,64>"
+    return f"sdpa_fwd_bf16_kernel<64,1,{2 if w.Lk <= 2048 else 3},128>"
+
+
 def bench_sdpa(args, w, rank, world, local_rank):
     import torch
     import transformer_head_scaled_03_gb300 as mha
@@ -925,7 +935,7 @@ def run_gpu(args):
         "roofline": {"bound": "tensor", "achieved": round(ach, 2), "peak": peak,
                      "unit": "TFLOP/s", "frac": round(ach / peak, 4),
                      "peak_source": f"{peak_src} bf16 burst", "traffic": traffic,
-                     "kernel": f"sdpa_fwd_bf16_kernel<{w.d},{2 if w.Lq > 128 else 1},{2 if w.d == 128 else 3}>"},
+                     "kernel": fwd_kernel_name(w)},
         "e2e": r["e2e"],
         "gpu_launches": args.steps,
         "clocks": r["clocks"],

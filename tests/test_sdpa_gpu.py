@@ -64,6 +64,12 @@ BF16_CASES = [
     (3, 2, 130, 256, 128, PAD, [256, 255, 1]),
     (3, 2, 256, 256, 64, PAD | CAUSAL, [1, 200, 256]),
     (2, 1, 384, 384, 128, PAD | CAUSAL, [383, 129]),
+    # each query tile of a two-tile CTA stops at its own diagonal (or at the
+    # key length, when that comes first)
+    (1, 2, 450, 450, 64, CAUSAL, None),
+    (2, 1, 450, 450, 128, CAUSAL, None),
+    (2, 3, 260, 260, 64, PAD | CAUSAL, [190, 65]),
+    (2, 2, 520, 520, 128, PAD | CAUSAL, [300, 520]),
 ]
 
 
@@ -160,11 +166,10 @@ def test_empty_batch_is_a_no_op():
     assert O.shape == (0, 2, 5, 64)
 
 
-# Shapes with more (b, h, query block) items than SMs and short key ranges:
-# the fused kernel runs one wave of CTAs that each work through a run of
-# items (the K/V ring, the Q buffers and every barrier phase carried from
-# one item to the next).  Causal runs mix block lengths; key padding gives
-# items of different lengths, including single-key and full-length ones.
+# Shapes with many more (b, h, query block) CTAs than SMs and short key
+# ranges: several waves, with CTAs of different lengths sharing an SM.
+# Causal runs mix block lengths; key padding gives items of different
+# lengths, including single-key and full-length ones.
 MULTI_ITEM_CASES = [
     # B, H, Lq, Lk, d, mask, lengths
     (40, 4, 700, 700, 64, CAUSAL, None),

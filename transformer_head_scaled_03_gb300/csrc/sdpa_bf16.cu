@@ -19,14 +19,15 @@
 //   warp 4*NQT         : TMA producer (Q once, then a ring of NST K and V
 //                        stages, 128-byte swizzled).
 //   warp 4*NQT+1       : MMA issuer (one thread) and TMEM owner.
-// Per key tile j and query tile t:
+// Per key tile j (BN = 128 or 64 keys) and query tile t:
 //   S_t  = Q_t K_j^T           tcgen05.mma, A and B from shared memory,
-//                              fp32 accumulator in TMEM (128 columns)
+//                              fp32 accumulator in TMEM (BN columns)
 //   P_t  = 2^(S_t*c - m*c)     softmax warps: tcgen05.ld of S, mask, online
 //                              max/sum, P packed to bf16 and tcgen05.st back
-//                              into the first 64 columns of S_t
+//                              into the first BN/2 columns of S_t
 //   O_t += P_t V_j             tcgen05.mma with A = P_t from TMEM and
 //                              B = V_j (MN-major) from shared memory
+// Under the causal mask each query tile stops at its own diagonal.
 // The epilogue divides O_t by l and stores bf16 or fp32, either as
 // [B,H,Lq,d] or directly in the concatenated-heads layout [B,Lq,H*d].
 #include <math.h>
@@ -38,7 +39,6 @@ namespace mha {
 namespace {
 
 constexpr int kBlockM = 128;      // query rows per tile = TMEM lanes
-constexpr int kBlockN = 128;      // keys per K/V tile
 constexpr int kSub = 128 * 128;   // bytes of a 128-row x 64-column bf16 block
 
 struct SdpaParams {
@@ -59,21 +59,32 @@ struct SdpaParams {
   float* lse;             // optional [B, H, Lq]: log2 of sum_j 2^(s_ij * scale_log2)
 };
 
-template <int D, int NQT, int NST>
+// BN = keys per K/V tile (128, or 64 to fit more query tiles in tensor
+// memory: each query tile holds BN columns of S and D columns of O).
+template <int D, int NQT, int NST, int BN = 128>
 struct Cfg {
   static_assert(D == 64 || D == 128, "head dim");
-  static constexpr int KB = D / 64;               // 64-column (128-byte) blocks per row
-  static constexpr int kTileBytes = KB * kSub;    // one 128-row tile of Q, K or V
+  static_assert(BN == 64 || BN == 128, "key tile");
+  static constexpr int KB = D / 64;                 // 64-column (128-byte) blocks per row
+  static constexpr int kQTileBytes = KB * kSub;     // one 128-row tile of Q
+  static constexpr int kKVBlock = BN * 128;         // one BN-row x 64-column block of K or V
+  static constexpr int kKVTileBytes = KB * kKVBlock;
   static constexpr int kSoftmaxWarps = 4 * NQT;
   static constexpr int kTmaWarp = kSoftmaxWarps;
   static constexpr int kMmaWarp = kSoftmaxWarps + 1;
   static constexpr int kThreads = 32 * (kSoftmaxWarps + 2);
-  static constexpr int kTmemNeed = NQT * (kBlockN + D);
-  static constexpr uint32_t kTmemCols = kTmemNeed <= 256 ? 256u : 512u;
+  static constexpr int kTmemNeed = NQT * (BN + D);
+  static constexpr uint32_t kTmemCols = kTmemNeed <= 128 ? 128u : kTmemNeed <= 256 ? 256u : 512u;
   static_assert(kTmemNeed <= 512, "TMEM budget");
+  // CTAs meant to share an SM: as many as tensor memory allows for the
+  // short-sequence d = 64 forms (their shared memory and registers are
+  // sized for it), one otherwise
+  static constexpr int kMinBlocks =
+      (D == 64 && NST == 2 && NQT == 1) ? static_cast<int>(512u / kTmemCols)
+      : (D == 64 && BN == 64) ? 2 : 1;
   // tensor-memory columns
-  __host__ __device__ static constexpr uint32_t tS(int t) { return static_cast<uint32_t>(t * kBlockN); }
-  __host__ __device__ static constexpr uint32_t tO(int t) { return static_cast<uint32_t>(NQT * kBlockN + t * D); }
+  __host__ __device__ static constexpr uint32_t tS(int t) { return static_cast<uint32_t>(t * BN); }
+  __host__ __device__ static constexpr uint32_t tO(int t) { return static_cast<uint32_t>(NQT * BN + t * D); }
   // barrier indices
   static constexpr int bQ = 0;
   __host__ __device__ static constexpr int bKF(int s) { return 1 + s; }
@@ -87,9 +98,9 @@ struct Cfg {
   static constexpr int kNumBars = bDrain + 1;
   // shared-memory layout from a 1024-byte aligned base
   static constexpr int kOffQ = 0;
-  static constexpr int kOffK = kOffQ + NQT * kTileBytes;
-  static constexpr int kOffV = kOffK + NST * kTileBytes;
-  static constexpr int kOffBar = kOffV + NST * kTileBytes;
+  static constexpr int kOffK = kOffQ + NQT * kQTileBytes;
+  static constexpr int kOffV = kOffK + NST * kKVTileBytes;
+  static constexpr int kOffBar = kOffV + NST * kKVTileBytes;
   static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
   static_assert(kSmemBytes <= 232448, "shared memory");
@@ -104,15 +115,12 @@ __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, uint64
   }
 }
 
-template <int D, int NQT, int NST, bool kAddMask, bool kLse>
-// The d = 64 single-tile, two-stage form is built for two CTAs per SM (80 KB
-// of shared memory, 256 TMEM columns and at most 168 registers each).
-__global__ void __launch_bounds__(Cfg<D, NQT, NST>::kThreads,
-                                  (D == 64 && NQT == 1 && NST == 2) ? 2 : 1)
+template <int D, int NQT, int NST, int BN, bool kAddMask, bool kLse>
+__global__ void __launch_bounds__(Cfg<D, NQT, NST, BN>::kThreads, Cfg<D, NQT, NST, BN>::kMinBlocks)
     sdpa_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ,
                          const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, const SdpaParams p) {
-  using C = Cfg<D, NQT, NST>;
+  using C = Cfg<D, NQT, NST, BN>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -176,15 +184,19 @@ __global__ void __launch_bounds__(Cfg<D, NQT, NST>::kThreads,
     if (L < 1 || L > p.Lk) bad_len = true;
     else key_end = L;
   }
-  int kv_stop = bad_len ? 0 : key_end;
-  if (causal) kv_stop = min(kv_stop, q0 + NQT * kBlockM);
-  const int n_kv = (kv_stop + kBlockN - 1) / kBlockN;
+  // key tiles that query tile t walks: up to its own diagonal when causal
+  auto n_kv_of = [&](int t) -> int {
+    int stop = bad_len ? 0 : key_end;
+    if (causal) stop = min(stop, q0 + (t + 1) * kBlockM);
+    return (stop + BN - 1) / BN;
+  };
+  const int n_kv = n_kv_of(NQT - 1);  // the most any tile of this CTA needs
   if (bad_len && threadIdx.x == 0) atomicOr(p.err, kErrKeyLength);
 
   if (warp == C::kTmaWarp) {
     // ------------------------------------------------------------ producer
     if (lane == 0 && n_kv > 0) {
-      mbar_expect_tx(bar(C::bQ), NQT * C::kTileBytes);
+      mbar_expect_tx(bar(C::bQ), NQT * C::kQTileBytes);
       for (int t = 0; t < NQT; ++t)
         for (int kb = 0; kb < C::KB; ++kb)
           tma_load_3d(base + C::kOffQ + (t * C::KB + kb) * kSub, &tmQ, bar(C::bQ), kb * 64,
@@ -194,16 +206,16 @@ __global__ void __launch_bounds__(Cfg<D, NQT, NST>::kThreads,
         const int st = j % NST;
         const uint32_t ph = (j / NST) & 1;
         if (!mbar_wait(bar(C::bKE(st)), ph ^ 1u, ctl)) break;
-        mbar_expect_tx(bar(C::bKF(st)), C::kTileBytes);
+        mbar_expect_tx(bar(C::bKF(st)), C::kKVTileBytes);
         for (int kb = 0; kb < C::KB; ++kb)
-          tma_load_3d(base + C::kOffK + (st * C::KB + kb) * kSub, &tmK, bar(C::bKF(st)),
-                      kb * 64, j * kBlockN, bh);
+          tma_load_3d(base + C::kOffK + (st * C::KB + kb) * C::kKVBlock, &tmK, bar(C::bKF(st)),
+                      kb * 64, j * BN, bh);
         k_issued = j + 1;
         if (!mbar_wait(bar(C::bVE(st)), ph ^ 1u, ctl)) break;
-        mbar_expect_tx(bar(C::bVF(st)), C::kTileBytes);
+        mbar_expect_tx(bar(C::bVF(st)), C::kKVTileBytes);
         for (int kb = 0; kb < C::KB; ++kb)
-          tma_load_3d(base + C::kOffV + (st * C::KB + kb) * kSub, &tmV, bar(C::bVF(st)),
-                      kb * 64, j * kBlockN, bh);
+          tma_load_3d(base + C::kOffV + (st * C::KB + kb) * C::kKVBlock, &tmV, bar(C::bVF(st)),
+                      kb * 64, j * BN, bh);
         v_issued = j + 1;
       }
       // let every issued copy land before the CTA can exit
@@ -222,31 +234,34 @@ __global__ void __launch_bounds__(Cfg<D, NQT, NST>::kThreads,
     // writes.  Each softmax warpgroup thus has two MMAs' time (the other
     // tile's PV and S) between S_t(j+1) landing and P_t(j+1) being needed.
     if (lane == 0 && n_kv > 0) {
-      constexpr uint32_t kIdescQK = idesc_bf16_f32(kBlockM, kBlockN, false, false);
+      constexpr uint32_t kIdescQK = idesc_bf16_f32(kBlockM, BN, false, false);
       constexpr uint32_t kIdescPV = idesc_bf16_f32(kBlockM, D, false, true);
       // Descriptors are built once; per MMA only a compile-time offset (in
       // 16-byte units, the descriptor's address granule) is added, which
       // keeps the single issuing thread off long integer chains.
       const uint64_t q_desc = sdesc_sw128(base + C::kOffQ, 16, 1024);
       const uint64_t k_desc = sdesc_sw128(base + C::kOffK, 16, 1024);
-      const uint64_t v_desc = sdesc_sw128(base + C::kOffV, kSub, 1024);
+      const uint64_t v_desc = sdesc_sw128(base + C::kOffV, C::kKVBlock, 1024);
       auto issue_qk = [&](int t, int st) {
-        const uint64_t qd = q_desc + static_cast<uint64_t>((t * C::kTileBytes) >> 4);
-        const uint64_t kd = k_desc + static_cast<uint64_t>((st * C::kTileBytes) >> 4);
+        const uint64_t qd = q_desc + static_cast<uint64_t>((t * C::kQTileBytes) >> 4);
+        const uint64_t kd = k_desc + static_cast<uint64_t>((st * C::kKVTileBytes) >> 4);
         const uint32_t d_tmem = tmem + C::tS(t);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
-          // 16 elements = 32 bytes inside a 128-byte row; 64-column blocks kSub apart
-          const uint64_t off = static_cast<uint64_t>(((ks >> 2) * kSub + (ks & 3) * 32) >> 4);
-          umma_ss(d_tmem, qd + off, kd + off, kIdescQK, ks > 0 ? 1u : 0u);
+          // 16 elements = 32 bytes inside a 128-byte row; the 64-column blocks
+          // are kSub apart in Q and kKVBlock apart in K
+          const uint64_t qoff = static_cast<uint64_t>(((ks >> 2) * kSub + (ks & 3) * 32) >> 4);
+          const uint64_t koff =
+              static_cast<uint64_t>(((ks >> 2) * C::kKVBlock + (ks & 3) * 32) >> 4);
+          umma_ss(d_tmem, qd + qoff, kd + koff, kIdescQK, ks > 0 ? 1u : 0u);
         }
       };
       auto issue_pv = [&](int t, int st, uint32_t accumulate) {
-        const uint64_t vd = v_desc + static_cast<uint64_t>((st * C::kTileBytes) >> 4);
+        const uint64_t vd = v_desc + static_cast<uint64_t>((st * C::kKVTileBytes) >> 4);
         const uint32_t d_tmem = tmem + C::tO(t);
         const uint32_t a_tmem = tmem + C::tS(t);
 #pragma unroll
-        for (int ks = 0; ks < kBlockN / 16; ++ks) {
+        for (int ks = 0; ks < BN / 16; ++ks) {
           // 16 keys of V = 16 rows of 128 bytes; P: 16 bf16 = 8 TMEM columns
           umma_ts(d_tmem, a_tmem + ks * 8, vd + static_cast<uint64_t>((ks * 16 * 128) >> 4),
                   kIdescPV, ks > 0 ? 1u : accumulate);
@@ -261,6 +276,9 @@ __global__ void __launch_bounds__(Cfg<D, NQT, NST>::kThreads,
         }
         umma_commit(bar(C::bKE(0)));
       }
+      // A query tile whose last key tile is j gets no S(j + 1); its output
+      // is complete after PV(j) and its epilogue runs while the other tile
+      // of the CTA (causal: the one further down) walks on.
       for (int j = 0; ok && j < n_kv; ++j) {
         const int st = j % NST;
         const uint32_t ph = (j / NST) & 1;
@@ -268,15 +286,19 @@ __global__ void __launch_bounds__(Cfg<D, NQT, NST>::kThreads,
         const int st1 = (j + 1) % NST;
         const uint32_t ph1 = ((j + 1) / NST) & 1;
         if (!(ok = mbar_wait(bar(C::bVF(st)), ph, ctl))) break;
+        bool k_ready = false;
         for (int t = 0; t < NQT && ok; ++t) {
+          const int n_t = n_kv_of(t);
+          if (j >= n_t) continue;
           if (!(ok = mbar_wait(bar(C::bP(t)), j & 1, ctl))) break;
           tc_fence_after();
           issue_pv(t, st, j > 0 ? 1u : 0u);
-          if (!more) {
+          if (j + 1 >= n_t) {
             umma_commit(bar(C::bO(t)));
             continue;
           }
-          if (t == 0 && !(ok = mbar_wait(bar(C::bKF(st1)), ph1, ctl))) break;
+          if (!k_ready && !(ok = mbar_wait(bar(C::bKF(st1)), ph1, ctl))) break;
+          k_ready = true;
           issue_qk(t, st1);
           umma_commit(bar(C::bS(t)));
         }
@@ -307,28 +329,27 @@ __global__ void __launch_bounds__(Cfg<D, NQT, NST>::kThreads,
     float m_ref = -INFINITY;
     float l = 0.f;
     bool ok = true;
-    for (int j = 0; j < n_kv; ++j) {
+    const int n_t = n_kv_of(t);
+    for (int j = 0; j < n_t; ++j) {
       if (!(ok = mbar_wait_warp(bar(C::bS(t)), j & 1, ctl))) break;
       tc_fence_after();
-      const int k0 = j * kBlockN;
-      const bool edge = (k0 + kBlockN > key_end) ||
-                        (causal && k0 + kBlockN - 1 > q0 + t * kBlockM);
+      const int k0 = j * BN;
+      const bool edge = (k0 + BN > key_end) || (causal && k0 + BN - 1 > q0 + t * kBlockM);
       // visible keys of this row in this tile: columns c <= last
       int last = key_end - 1 - k0;
       if (causal) last = min(last, q_row - k0);
       // S row -> registers (masked)
-      auto load_scores = [&](float (&x)[128]) {
-        uint32_t s[128];
-        tmem_ld32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
-        tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
-        tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(&s[64]));
-        tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(&s[96]));
+      auto load_scores = [&](float (&x)[BN]) {
+        uint32_t s[BN];
+#pragma unroll
+        for (int c = 0; c < BN; c += 32)
+          tmem_ld32(tS + c, *reinterpret_cast<uint32_t(*)[32]>(&s[c]));
         tmem_ld_wait(s);
 #pragma unroll
-        for (int c = 0; c < 128; ++c) x[c] = __uint_as_float(s[c]);
+        for (int c = 0; c < BN; ++c) x[c] = __uint_as_float(s[c]);
         if (edge) {
 #pragma unroll
-          for (int c = 0; c < 128; ++c) x[c] = c <= last ? x[c] : -INFINITY;
+          for (int c = 0; c < BN; ++c) x[c] = c <= last ? x[c] : -INFINITY;
         }
         if constexpr (kAddMask) {
           // additive float mask, in raw-score units (M / scale); -inf blocks
@@ -336,10 +357,10 @@ __global__ void __launch_bounds__(Cfg<D, NQT, NST>::kThreads,
             const float* mrow = p.add_mask + static_cast<int64_t>(b) * p.mask_sb +
                                 static_cast<int64_t>(h) * p.mask_sh +
                                 static_cast<int64_t>(q_row) * p.Lk + k0;
-            const int nvalid = min(kBlockN, p.Lk - k0);
-            if (p.mask_vec && nvalid == kBlockN) {
+            const int nvalid = min(BN, p.Lk - k0);
+            if (p.mask_vec && nvalid == BN) {
 #pragma unroll
-              for (int c = 0; c < 128; c += 4) {
+              for (int c = 0; c < BN; c += 4) {
                 const float4 mv = __ldg(reinterpret_cast<const float4*>(mrow + c));
                 x[c] = fmaf(mv.x, p.inv_scale, x[c]);
                 x[c + 1] = fmaf(mv.y, p.inv_scale, x[c + 1]);
@@ -348,43 +369,43 @@ __global__ void __launch_bounds__(Cfg<D, NQT, NST>::kThreads,
               }
             } else {
 #pragma unroll
-              for (int c = 0; c < 128; ++c)
+              for (int c = 0; c < BN; ++c)
                 if (c < nvalid) x[c] = fmaf(__ldg(mrow + c), p.inv_scale, x[c]);
             }
           }
         }
       };
       // tile maximum: eight independent 3-input max chains, then combine
-      auto tile_max = [&](const float (&x)[128]) -> float {
+      auto tile_max = [&](const float (&x)[BN]) -> float {
         float m8[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) m8[i] = fmax3(x[i], x[8 + i], x[16 + i]);
 #pragma unroll
-        for (int c = 24; c < 120; c += 16)
+        for (int c = 24; c < BN - 8; c += 16)
 #pragma unroll
           for (int i = 0; i < 8; ++i) m8[i] = fmax3(m8[i], x[c + i], x[c + 8 + i]);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) m8[i] = fmaxf(m8[i], x[120 + i]);
+        for (int i = 0; i < 8; ++i) m8[i] = fmaxf(m8[i], x[BN - 8 + i]);
         return fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]),
                      fmaxf(m8[6], m8[7]));
       };
       // p = 2^(s*sl2 - mb), two at a time with four independent partial sums
-      auto exps = [&](const float (&x)[128], float mb, float2 (&acc)[4], uint32_t (&pk)[64]) {
+      auto exps = [&](const float (&x)[BN], float mb, float2 (&acc)[4], uint32_t (&pk)[BN / 2]) {
         const float2 scale2 = make_float2(sl2, sl2);
         const float2 shift2 = make_float2(-mb, -mb);
 #pragma unroll
         for (int i = 0; i < 4; ++i) acc[i] = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
+        for (int c = 0; c < BN / 2; ++c) {
           const float2 e = ffma2(make_float2(x[2 * c], x[2 * c + 1]), scale2, shift2);
           const float2 pp = make_float2(ex2_approx(e.x), ex2_approx(e.y));
           acc[c & 3] = fadd2(acc[c & 3], pp);
           pk[c] = pack_bf16x2(pp.x, pp.y);
         }
       };
-      float x[128];
+      float x[BN];
       float2 acc[4];
-      uint32_t pk[64];
+      uint32_t pk[BN / 2];
       float alpha = 1.f;
       load_scores(x);
       const float mt = tile_max(x);
@@ -397,8 +418,9 @@ __global__ void __launch_bounds__(Cfg<D, NQT, NST>::kThreads,
       const float2 a01 = fadd2(acc[0], acc[1]), a23 = fadd2(acc[2], acc[3]);
       const float2 a = fadd2(a01, a23);
       l += a.x + a.y;
-      tmem_st32(tS + 0, *reinterpret_cast<const uint32_t(*)[32]>(&pk[0]));
-      tmem_st32(tS + 32, *reinterpret_cast<const uint32_t(*)[32]>(&pk[32]));
+#pragma unroll
+      for (int c = 0; c < BN / 2; c += 32)
+        tmem_st32(tS + c, *reinterpret_cast<const uint32_t(*)[32]>(&pk[c]));
       // Rescale the partial output when the reference max moved.  P.V of the
       // previous tile is complete: it was issued before this tile's S, whose
       // commit covers it.  Done after P is stored, when the score registers
@@ -419,7 +441,7 @@ __global__ void __launch_bounds__(Cfg<D, NQT, NST>::kThreads,
       mbar_arrive(bar(C::bP(t)));
     }
     // ------------------------------------------------------------ epilogue
-    bool have = ok && n_kv > 0;
+    bool have = ok && n_t > 0;
     if (have) {
       have = mbar_wait_warp(bar(C::bO(t)), 0, ctl);
       tc_fence_after();
@@ -483,9 +505,9 @@ __global__ void __launch_bounds__(Cfg<D, NQT, NST>::kThreads,
   if (warp == C::kMmaWarp) tmem_dealloc<C::kTmemCols>(tmem);
 }
 
-template <int D, int NQT, int NST, bool kAddMask, bool kLse = false>
+template <int D, int NQT, int NST, bool kAddMask, bool kLse = false, int BN = 128>
 cudaError_t launch_impl(const SdpaArgs& a, const DeviceCtl& ctl) {
-  using C = Cfg<D, NQT, NST>;
+  using C = Cfg<D, NQT, NST, BN>;
   CUtensorMap maps[3];
   const void* ptrs[3] = {a.Q, a.K, a.V};
   const int lens[3] = {a.Lq, a.Lk, a.Lk};
@@ -494,7 +516,7 @@ cudaError_t launch_impl(const SdpaArgs& a, const DeviceCtl& ctl) {
                               static_cast<uint64_t>(a.B) * a.H};
     const uint64_t strides[2] = {static_cast<uint64_t>(D) * 2,
                                  static_cast<uint64_t>(lens[i]) * D * 2};
-    const uint32_t box[3] = {64, 128, 1};
+    const uint32_t box[3] = {64, i == 0 ? 128u : static_cast<uint32_t>(BN), 1};
     if (!encode_tensor_map(&maps[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
                            const_cast<void*>(ptrs[i]), dims, strides, box,
                            CU_TENSOR_MAP_SWIZZLE_128B))
@@ -524,7 +546,7 @@ cudaError_t launch_impl(const SdpaArgs& a, const DeviceCtl& ctl) {
   const long long grid = static_cast<long long>(p.num_q_blocks) * a.B * a.H;
   if (grid <= 0) return cudaSuccess;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  auto kern = sdpa_fwd_bf16_kernel<D, NQT, NST, kAddMask, kLse>;
+  auto kern = sdpa_fwd_bf16_kernel<D, NQT, NST, BN, kAddMask, kLse>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
@@ -538,11 +560,14 @@ cudaError_t launch_impl(const SdpaArgs& a, const DeviceCtl& ctl) {
 
 cudaError_t launch_sdpa_bf16(const SdpaArgs& a, const DeviceCtl& ctl) {
   // Two query tiles per CTA share every K/V tile (half the K/V traffic per
-  // query row); a single tile when there are too few rows to fill two.
+  // query row); a single tile when there are too few rows to fill two.  At
+  // d = 64 every two-tile form (plain, additive mask, row log-sum-exp) uses
+  // 64-key tiles, so the three give bit-identical outputs.
   const bool two = a.Lq > kBlockM;
   if (a.add_mask) {
     if (a.d == 64)
-      return two ? launch_impl<64, 2, 3, true>(a, ctl) : launch_impl<64, 1, 3, true>(a, ctl);
+      return two ? launch_impl<64, 2, 3, true, false, 64>(a, ctl)
+                 : launch_impl<64, 1, 3, true>(a, ctl);
     if (a.d == 128)
       return two ? launch_impl<128, 2, 2, true>(a, ctl) : launch_impl<128, 1, 2, true>(a, ctl);
     return cudaErrorInvalidValue;
@@ -551,19 +576,20 @@ cudaError_t launch_sdpa_bf16(const SdpaArgs& a, const DeviceCtl& ctl) {
   // forward's code is unchanged by it
   if (a.lse != nullptr) {
     if (a.d == 64)
-      return two ? launch_impl<64, 2, 3, false, true>(a, ctl)
+      return two ? launch_impl<64, 2, 3, false, true, 64>(a, ctl)
                  : launch_impl<64, 1, 3, false, true>(a, ctl);
     if (a.d == 128)
       return two ? launch_impl<128, 2, 2, false, true>(a, ctl)
                  : launch_impl<128, 1, 2, false, true>(a, ctl);
     return cudaErrorInvalidValue;
   }
-  // d = 64 with at most 16 key tiles: one query tile per CTA and two CTAs per
-  // SM, so one CTA's pipeline fill and epilogue overlap the other's tiles
-  // (measured faster up to Lk = 2048, slower from 8192 on)
+  // d = 64: two query tiles per CTA on 64-key tiles, so that a query tile
+  // needs 128 TMEM columns and two CTAs share an SM: four query tiles (four
+  // softmax/MMA chains) per SM instead of two.  A lone query tile keeps the
+  // 128-key form, two CTAs per SM (measured faster for Lq <= 128).
+  if (a.d == 64 && two) return launch_impl<64, 2, 3, false, false, 64>(a, ctl);
   if (a.d == 64 && a.Lk <= 2048) return launch_impl<64, 1, 2, false>(a, ctl);
-  if (a.d == 64)
-    return two ? launch_impl<64, 2, 3, false>(a, ctl) : launch_impl<64, 1, 3, false>(a, ctl);
+  if (a.d == 64) return launch_impl<64, 1, 3, false>(a, ctl);
   if (a.d == 128)
     return two ? launch_impl<128, 2, 2, false>(a, ctl) : launch_impl<128, 1, 2, false>(a, ctl);
   return cudaErrorInvalidValue;
