@@ -104,6 +104,14 @@ class Workload:
             return 4.0 * H * Lq * d * float(np.sum(key_lengths))
         return 4.0 * B * H * Lq * Lk * d
 
+    def sdpa_bytes(self, key_lengths=None) -> float:
+        """Minimum HBM bytes of one attention forward (bf16): Q read and O
+        written once, and every key and value row that some query may see
+        read once (rows at or past len_b are never read under key padding)."""
+        kv_rows = (float(np.sum(key_lengths)) if self.mask & MASK_KEY_PADDING
+                   and key_lengths is not None else float(self.B * self.Lk))
+        return 2.0 * self.H * self.d * (2.0 * self.B * self.Lq + 2.0 * kv_rows)
+
     def decode_bytes(self, key_lengths=None) -> float:
         """Algorithmic HBM bytes of one decode pass (bf16): every held key and
         value row read once, the queries read and the outputs written once."""
