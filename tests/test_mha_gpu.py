@@ -53,6 +53,12 @@ CASES = [
     (torch.float32, 1, 128, 128, 512, 8, NONE, None, False),
     (torch.float32, 2, 70, 70, 96, 3, CAUSAL, None, False),
     (torch.float32, 2, 33, 90, 128, 4, PAD, [90, 5], True),
+    # fp32 projections in both GEMM forms and both load paths: 32 x 64 tiles
+    # (enough rows to fill the GPU) and the split-k 16 x 32 tiles, with
+    # D a multiple of 4 (16-byte copies) and not (element loads; d = 30)
+    (torch.float32, 8, 512, 512, 256, 4, NONE, None, False),
+    (torch.float32, 4, 300, 300, 90, 3, NONE, None, False),
+    (torch.float32, 3, 50, 70, 90, 3, PAD, [70, 1, 33], True),
 ]
 
 

@@ -1,10 +1,12 @@
 // fp32_path.cu -- fp32 CUDA-core kernels for callers that need fp32
 // accuracy (max |err| ~1e-6 against an fp64 reference, where bf16 or TF32
 // tensor-core inputs would not do):
-//   * scaled dot-product attention, one warp per query row at a time, lane j
-//     scoring key j of a 32-key chunk held in shared memory, the row max and
-//     row sum reduced with warp shuffles, online over the chunks;
-//   * a 64x64-tiled GEMM C = A @ W with the head-split or row-major store.
+//   * scaled dot-product attention, one warp per two query rows, lane j
+//     scoring keys j and j + 32 of a 64-key chunk held in shared memory, the
+//     row max and row sum reduced with warp shuffles, online over the chunks;
+//   * a tiled GEMM C = A @ W with the head-split or row-major store (32 x 64
+//     tiles, or 16 x 32 tiles with the k-steps split inside the CTA for
+//     problems too small to fill the GPU).
 // Formulas as in sdpa_bf16.cu: "How Transformers Work" (worksonmygpu.com),
 // "Scaled dot-product attention"; "The Transformer" (rayaq.ca), "Masks: who
 // may look at whom"; projections y = x @ W as in "32 Transformer"
@@ -18,8 +20,8 @@ namespace mha {
 namespace {
 
 constexpr int kKeys = 64;   // keys per shared-memory chunk (two per lane)
-constexpr int kRowsW = 4;   // query rows per warp, processed together
-constexpr int kWarps = 4;   // warps per CTA
+constexpr int kRowsW = 2;   // query rows per warp, processed together
+constexpr int kWarps = 8;   // warps per CTA
 constexpr int kRowsC = kRowsW * kWarps;
 
 struct SdpaF32Params {
@@ -37,6 +39,20 @@ struct SdpaF32Params {
   int64_t mask_sb, mask_sh;
 };
 
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
@@ -48,17 +64,22 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-// One CTA = 16 query rows of one (b, h); warp w owns rows 4w..4w+3 and
+// One CTA = 16 query rows of one (b, h); warp w owns rows 2w, 2w+1 and
 // scores them together against each 64-key chunk (lane j: keys j and j+32),
-// so every K and V element read from shared memory serves four rows.
+// so every K and V element read from shared memory serves two rows.  Eight
+// warps per CTA keep two warps per scheduler busy on the short layers this
+// path serves.  The
+// chunks stream through two shared-memory stages by cp.async: chunk c + 1 is
+// in flight while chunk c is scored, and the first two are requested before
+// Q is read, so the load latencies of a short key range overlap.
 // DP: head-dim bound (d <= DP, DP in {32, 64, 128}).
 template <int DP>
 __global__ void __launch_bounds__(kWarps * 32) sdpa_f32_kernel(const SdpaF32Params p) {
   constexpr int CPL = DP / 32;  // output columns per lane
   extern __shared__ __align__(16) float fsm[];
   float* sQ = fsm;                              // [kRowsC][DP]
-  float* sK = sQ + kRowsC * DP;                 // [kKeys][DP + 1]
-  float* sV = sK + kKeys * (DP + 1);            // [kKeys][DP]
+  float* sK0 = sQ + kRowsC * DP;                // two stages of [kKeys][DP + 1]
+  float* sV0 = sK0 + 2 * kKeys * (DP + 1);      // two stages of [kKeys][DP]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int row0 = blockIdx.x * kRowsC;
   const int h = blockIdx.y, b = blockIdx.z;
@@ -76,6 +97,49 @@ __global__ void __launch_bounds__(kWarps * 32) sdpa_f32_kernel(const SdpaF32Para
   int kv_stop = bad_len ? 0 : key_end;
   if (causal) kv_stop = min(kv_stop, row0 + kRowsC);
 
+  // key chunk c (keys c*kKeys ..) -> stage c & 1; rows past Lk and columns
+  // past d are zero-filled.  V goes in 16-byte pieces when its rows allow
+  // (d a multiple of 4, 16-byte aligned base).
+  const bool v_vec = (d % 4 == 0) && (reinterpret_cast<uintptr_t>(p.V) & 15u) == 0;
+  auto load_chunk = [&](int chunk) {
+    float* sK = sK0 + (chunk & 1) * kKeys * (DP + 1);
+    float* sV = sV0 + (chunk & 1) * kKeys * DP;
+    const int k0 = chunk * kKeys;
+    for (int idx = threadIdx.x; idx < kKeys * DP; idx += blockDim.x) {
+      const int j = idx / DP, c = idx % DP;
+      const int key = k0 + j;
+      const bool in = key < p.Lk && c < d;
+      const size_t g = in ? (bh * p.Lk + key) * d + c : 0;
+      // K rows are padded to DP + 1 floats (conflict-free column reads), so
+      // they go element by element
+      cp_async4(static_cast<uint32_t>(__cvta_generic_to_shared(sK + j * (DP + 1) + c)), p.K + g,
+                in ? 4u : 0u);
+    }
+    if (v_vec) {  // V rows: 16-byte pieces
+      for (int idx = threadIdx.x; idx < kKeys * DP / 4; idx += blockDim.x) {
+        const int j = idx / (DP / 4), c = (idx % (DP / 4)) * 4;
+        const int key = k0 + j;
+        const bool in = key < p.Lk && c < d;
+        const size_t g = in ? (bh * p.Lk + key) * d + c : 0;
+        cp_async16(static_cast<uint32_t>(__cvta_generic_to_shared(sV + j * DP + c)), p.V + g,
+                   in ? 16u : 0u);
+      }
+    } else {
+      for (int idx = threadIdx.x; idx < kKeys * DP; idx += blockDim.x) {
+        const int j = idx / DP, c = idx % DP;
+        const int key = k0 + j;
+        const bool in = key < p.Lk && c < d;
+        const size_t g = in ? (bh * p.Lk + key) * d + c : 0;
+        cp_async4(static_cast<uint32_t>(__cvta_generic_to_shared(sV + j * DP + c)), p.V + g,
+                  in ? 4u : 0u);
+      }
+    }
+  };
+  const int n_chunks = (kv_stop + kKeys - 1) / kKeys;
+  if (n_chunks > 0) load_chunk(0);
+  cp_async_commit();
+  if (n_chunks > 1) load_chunk(1);
+  cp_async_commit();
   for (int idx = threadIdx.x; idx < kRowsC * DP; idx += blockDim.x) {
     const int r = idx / DP, c = idx % DP;
     const int q = row0 + r;
@@ -90,15 +154,11 @@ __global__ void __launch_bounds__(kWarps * 32) sdpa_f32_kernel(const SdpaF32Para
     for (int cc = 0; cc < CPL; ++cc) o[i][cc] = 0.f;
   }
   const float* q_rows = sQ + warp * kRowsW * DP;
-  for (int k0 = 0; k0 < kv_stop; k0 += kKeys) {
-    __syncthreads();
-    for (int idx = threadIdx.x; idx < kKeys * DP; idx += blockDim.x) {
-      const int j = idx / DP, c = idx % DP;
-      const int key = k0 + j;
-      const bool in = key < p.Lk && c < d;
-      sK[j * (DP + 1) + c] = in ? p.K[(bh * p.Lk + key) * d + c] : 0.f;
-      sV[j * DP + c] = in ? p.V[(bh * p.Lk + key) * d + c] : 0.f;
-    }
+  for (int chunk = 0; chunk < n_chunks; ++chunk) {
+    const int k0 = chunk * kKeys;
+    const float* sK = sK0 + (chunk & 1) * kKeys * (DP + 1);
+    const float* sV = sV0 + (chunk & 1) * kKeys * DP;
+    cp_async_wait<1>();  // this chunk has landed (the next may be in flight)
     __syncthreads();
     // scores s[i][t] of row i against key k0 + lane + 32 t (Q pre-scaled)
     float s[kRowsW][2];
@@ -159,7 +219,11 @@ __global__ void __launch_bounds__(kWarps * 32) sdpa_f32_kernel(const SdpaF32Para
         }
       }
     }
+    __syncthreads();  // every warp is done with this stage before it is refilled
+    if (chunk + 2 < n_chunks) load_chunk(chunk + 2);
+    cp_async_commit();
   }
+  cp_async_wait<0>();
 #pragma unroll
   for (int i = 0; i < kRowsW; ++i) {
     const int q_row = row0 + warp * kRowsW + i;
@@ -178,11 +242,13 @@ __global__ void __launch_bounds__(kWarps * 32) sdpa_f32_kernel(const SdpaF32Para
 // ------------------------------------------------------------------ GEMM
 //
 // C = A[M,K] @ W[K,N] in fp32 FFMA.  CTA tile 32 x 64, k-step 32, 256
-// threads, each owning 2 rows x 4 columns; both operand tiles are staged in
-// shared memory by cp.async through a two-stage ring so the next k-step's
-// loads are in flight while the current one is multiplied.  When K or N is
-// not a multiple of 4 (no 16-byte chunks), the tiles are filled by plain
-// loads instead.
+// threads, each owning 2 rows x 4 columns (the small-M form below serves
+// problems that would leave SMs idle).  Both operand tiles are staged in
+// shared memory by cp.async through a ring of kStages k-steps, so that
+// kStages - 1 k-steps of loads are in flight while one is multiplied: with
+// K = 512 a k-step is a few hundred cycles of arithmetic, well under the
+// latency of an L2 or HBM load.  When K or N is not a multiple of 4 (no
+// 16-byte chunks), the tiles are filled by plain loads instead.
 
 struct GemmF32Params {
   const float* A[3];
@@ -196,30 +262,33 @@ struct GemmF32Params {
   int M, N, K;
 };
 
-constexpr int kBM = 32, kBN = 64, kBK = 32;
+constexpr int kBM = 32, kBK = 32;
 constexpr int kApad = kBK + 4;  // A rows of 36 floats: 16-byte aligned, conflict-free column reads
+constexpr int kStages = 4;
+constexpr int kSplitBM = 16;  // rows of the small-M form's tiles
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+
+template <int BN>
+constexpr int gemm_f32_smem() {
+  return kStages * (kBM * kApad + kBK * BN) * 4;
 }
 
-template <bool kVec>
+template <bool kVec, int BN>
 __global__ void __launch_bounds__(256) gemm_f32_kernel(const GemmF32Params p) {
-  __shared__ __align__(16) float As[2][kBM][kApad];
-  __shared__ __align__(16) float Ws[2][kBK][kBN];
+  constexpr int TX = BN / 4;         // threads across the columns (4 columns each)
+  constexpr int TY = 256 / TX;       // threads down the rows
+  constexpr int RM = kBM / TY;       // rows per thread
+  static_assert(RM * TY == kBM && TX * TY == 256, "thread layout");
+  extern __shared__ __align__(16) float gsm[];
+  float (*As)[kBM][kApad] = reinterpret_cast<float (*)[kBM][kApad]>(gsm);
+  float (*Ws)[kBK][BN] = reinterpret_cast<float (*)[kBK][BN]>(gsm + kStages * kBM * kApad);
   const int z = blockIdx.z;
   const float* __restrict__ A = p.A[z];
   const float* __restrict__ W = p.W[z];
   const int M = p.M, N = p.N, K = p.K;
-  const int m0 = blockIdx.y * kBM, n0 = blockIdx.x * kBN;
+  const int m0 = blockIdx.y * kBM, n0 = blockIdx.x * BN;
   const int tid = threadIdx.x;
-  const int tx = tid & 15, ty = tid >> 4;  // columns 4*tx.., rows 2*ty..
+  const int tx = tid % TX, ty = tid / TX;  // columns 4*tx.., rows RM*ty..
   const int num_k = (K + kBK - 1) / kBK;
 
   auto load_tile = [&](int kt, int buf) {
@@ -233,9 +302,9 @@ __global__ void __launch_bounds__(256) gemm_f32_kernel(const GemmF32Params p) {
                    in ? A + static_cast<size_t>(gm) * K + gk : A, in ? 16u : 0u);
       }
 #pragma unroll
-      for (int i = 0; i < 2; ++i) {  // W: 32 rows x 16 chunks, two per thread
+      for (int i = 0; i < BN / 32; ++i) {  // W: 32 rows x BN/4 chunks
         const int idx = tid + 256 * i;
-        const int r = idx >> 4, c4 = (idx & 15) * 4;
+        const int r = idx / TX, c4 = (idx % TX) * 4;
         const int gk = k0 + r, gn = n0 + c4;
         const bool in = gk < K && gn < N;
         cp_async16(static_cast<uint32_t>(__cvta_generic_to_shared(&Ws[buf][r][c4])),
@@ -250,52 +319,52 @@ __global__ void __launch_bounds__(256) gemm_f32_kernel(const GemmF32Params p) {
         As[buf][r][c] = (gm < M && gk < K) ? A[static_cast<size_t>(gm) * K + gk] : 0.f;
       }
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
+      for (int i = 0; i < BN / 8; ++i) {
         const int idx = tid + 256 * i;
-        const int r = idx >> 6, c = idx & 63;
+        const int r = idx / BN, c = idx % BN;
         const int gk = k0 + r, gn = n0 + c;
         Ws[buf][r][c] = (gk < K && gn < N) ? W[static_cast<size_t>(gk) * N + gn] : 0.f;
       }
     }
   };
 
-  float acc[2][4] = {};
-  load_tile(0, 0);
-  if constexpr (kVec) cp_async_commit();
+  float acc[RM][4] = {};
+  // prologue: the first kStages - 1 k-steps in flight (empty groups keep the
+  // group count in step when K is short)
+#pragma unroll
+  for (int s = 0; s < kStages - 1; ++s) {
+    if (s < num_k) load_tile(s, s);
+    if constexpr (kVec) cp_async_commit();
+  }
   for (int kt = 0; kt < num_k; ++kt) {
-    const int buf = kt & 1;
-    if (kt + 1 < num_k) {
-      load_tile(kt + 1, buf ^ 1);
-      if constexpr (kVec) {
-        cp_async_commit();
-        cp_async_wait<1>();  // tile kt has landed; kt+1 may still be in flight
-      }
-    } else if constexpr (kVec) {
-      cp_async_wait<0>();
+    const int buf = kt % kStages;
+    if constexpr (kVec) cp_async_wait<kStages - 2>();  // k-step kt has landed
+    __syncthreads();  // ... for every thread; and the buffer refilled below is free
+    {
+      const int kn = kt + kStages - 1;
+      if (kn < num_k) load_tile(kn, kn % kStages);
+      if constexpr (kVec) cp_async_commit();
     }
-    __syncthreads();
 #pragma unroll
     for (int kk = 0; kk < kBK; ++kk) {
-      const float a0 = As[buf][2 * ty][kk], a1 = As[buf][2 * ty + 1][kk];
       const float4 w = *reinterpret_cast<const float4*>(&Ws[buf][kk][4 * tx]);
-      acc[0][0] = fmaf(a0, w.x, acc[0][0]);
-      acc[0][1] = fmaf(a0, w.y, acc[0][1]);
-      acc[0][2] = fmaf(a0, w.z, acc[0][2]);
-      acc[0][3] = fmaf(a0, w.w, acc[0][3]);
-      acc[1][0] = fmaf(a1, w.x, acc[1][0]);
-      acc[1][1] = fmaf(a1, w.y, acc[1][1]);
-      acc[1][2] = fmaf(a1, w.z, acc[1][2]);
-      acc[1][3] = fmaf(a1, w.w, acc[1][3]);
+#pragma unroll
+      for (int i = 0; i < RM; ++i) {
+        const float a = As[buf][RM * ty + i][kk];
+        acc[i][0] = fmaf(a, w.x, acc[i][0]);
+        acc[i][1] = fmaf(a, w.y, acc[i][1]);
+        acc[i][2] = fmaf(a, w.z, acc[i][2]);
+        acc[i][3] = fmaf(a, w.w, acc[i][3]);
+      }
     }
-    __syncthreads();  // the buffer is refilled two k-steps later
   }
   float* C = p.C[z];
   const bool split = p.store[z] == static_cast<int>(GemmStore::kHeadSplit);
   const float* bias = p.bias[z];
   const bool relu = p.relu[z] != 0;
 #pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const int m = m0 + 2 * ty + i;
+  for (int i = 0; i < RM; ++i) {
+    const int m = m0 + RM * ty + i;
     if (m >= M) continue;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -315,6 +384,147 @@ __global__ void __launch_bounds__(256) gemm_f32_kernel(const GemmF32Params p) {
       C[off] = v;
     }
   }
+}
+
+// Small-M form: BM x 32 CTA tiles with the k-step split four ways inside the
+// CTA.  The 256 threads are four groups of 64; group g multiplies k-columns
+// 8g..8g+7 of every staged k-step, each thread a (BM / 8) x 4 block of the
+// tile (rows ty, ty+8, ...: conflict-free A reads).  The four partial
+// tiles are summed through shared memory at the end, in a fixed order.  It
+// puts four times as many warps on each output tile as the plain form, for
+// problems too small to fill the GPU with CTAs (a 128-row layer).
+template <bool kVec, int BM>
+__global__ void __launch_bounds__(256) gemm_f32_splitk_kernel(const GemmF32Params p) {
+  constexpr int BN = 32;
+  constexpr int RM = BM / 8;  // rows per thread
+  extern __shared__ __align__(16) float gsm[];
+  float (*As)[BM][kApad] = reinterpret_cast<float (*)[BM][kApad]>(gsm);
+  float (*Ws)[kBK][BN] = reinterpret_cast<float (*)[kBK][BN]>(gsm + kStages * BM * kApad);
+  const int z = blockIdx.z;
+  const float* __restrict__ A = p.A[z];
+  const float* __restrict__ W = p.W[z];
+  const int M = p.M, N = p.N, K = p.K;
+  const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
+  const int tid = threadIdx.x;
+  const int grp = tid >> 6, t = tid & 63;
+  const int ty = t >> 3, tx = t & 7;  // rows ty + 8i, columns 4tx..4tx+3
+  const int num_k = (K + kBK - 1) / kBK;
+
+  auto load_tile = [&](int kt, int buf) {
+    const int k0 = kt * kBK;
+    if constexpr (kVec) {
+      if (tid < BM * 8) {  // A: BM rows x 8 chunks of 4 floats
+        const int r = tid >> 3, c4 = (tid & 7) * 4;
+        const int gm = m0 + r, gk = k0 + c4;
+        const bool in = gm < M && gk < K;
+        cp_async16(static_cast<uint32_t>(__cvta_generic_to_shared(&As[buf][r][c4])),
+                   in ? A + static_cast<size_t>(gm) * K + gk : A, in ? 16u : 0u);
+      }
+      {  // W: 32 rows x 8 chunks
+        const int r = tid >> 3, c4 = (tid & 7) * 4;
+        const int gk = k0 + r, gn = n0 + c4;
+        const bool in = gk < K && gn < N;
+        cp_async16(static_cast<uint32_t>(__cvta_generic_to_shared(&Ws[buf][r][c4])),
+                   in ? W + static_cast<size_t>(gk) * N + gn : W, in ? 16u : 0u);
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int idx = tid + 256 * i;
+        const int r = idx >> 5, c = idx & 31;
+        if (r < BM) {
+          const int gm = m0 + r, gk = k0 + c;
+          As[buf][r][c] = (gm < M && gk < K) ? A[static_cast<size_t>(gm) * K + gk] : 0.f;
+        }
+        const int gk2 = k0 + r, gn = n0 + c;
+        Ws[buf][r][c] = (gk2 < K && gn < N) ? W[static_cast<size_t>(gk2) * N + gn] : 0.f;
+      }
+    }
+  };
+
+  float acc[RM][4] = {};
+#pragma unroll
+  for (int st = 0; st < kStages - 1; ++st) {
+    if (st < num_k) load_tile(st, st);
+    if constexpr (kVec) cp_async_commit();
+  }
+  for (int kt = 0; kt < num_k; ++kt) {
+    const int buf = kt % kStages;
+    if constexpr (kVec) cp_async_wait<kStages - 2>();
+    __syncthreads();
+    {
+      const int kn = kt + kStages - 1;
+      if (kn < num_k) load_tile(kn, kn % kStages);
+      if constexpr (kVec) cp_async_commit();
+    }
+#pragma unroll
+    for (int kk = grp * 8; kk < grp * 8 + 8; ++kk) {
+      const float4 w = *reinterpret_cast<const float4*>(&Ws[buf][kk][4 * tx]);
+#pragma unroll
+      for (int i = 0; i < RM; ++i) {
+        const float a = As[buf][ty + 8 * i][kk];
+        acc[i][0] = fmaf(a, w.x, acc[i][0]);
+        acc[i][1] = fmaf(a, w.y, acc[i][1]);
+        acc[i][2] = fmaf(a, w.z, acc[i][2]);
+        acc[i][3] = fmaf(a, w.w, acc[i][3]);
+      }
+    }
+  }
+  if constexpr (kVec) cp_async_wait<0>();
+  __syncthreads();  // the stages are free: reuse them for the four partial tiles
+  float (*red)[BM][BN + 1] = reinterpret_cast<float (*)[BM][BN + 1]>(gsm);
+#pragma unroll
+  for (int i = 0; i < RM; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) red[grp][ty + 8 * i][4 * tx + j] = acc[i][j];
+  __syncthreads();
+  float* C = p.C[z];
+  const bool split = p.store[z] == static_cast<int>(GemmStore::kHeadSplit);
+  const float* bias = p.bias[z];
+  const bool relu = p.relu[z] != 0;
+#pragma unroll
+  for (int e = 0; e < BM / 8; ++e) {
+    const int o = tid + 256 * e;
+    const int r = o >> 5, c = o & 31;
+    const int m = m0 + r, n = n0 + c;
+    if (m >= M || n >= N) continue;
+    float v = (red[0][r][c] + red[1][r][c]) + (red[2][r][c] + red[3][r][c]);
+    size_t off;
+    if (split) {
+      const int L = p.L[z], dh = p.dh[z];
+      const int bb = m / L, l = m - bb * L, hh = n / dh, cc = n - hh * dh;
+      off = ((static_cast<size_t>(bb) * (N / dh) + hh) * L + l) * dh + cc;
+    } else {
+      off = static_cast<size_t>(m) * N + n;
+    }
+    if (bias) v += bias[n];
+    if (relu) v = fmaxf(v, 0.f);
+    C[off] = v;
+  }
+}
+
+template <bool kVec>
+cudaError_t launch_gemm_f32_splitk(const GemmF32Params& p, int count, cudaStream_t s) {
+  constexpr int BM = kSplitBM;
+  const dim3 grid((p.N + 31) / 32, (p.M + BM - 1) / BM, count);
+  auto kern = gemm_f32_splitk_kernel<kVec, BM>;
+  constexpr int smem = kStages * (BM * kApad + kBK * 32) * 4;
+  static_assert(smem >= 4 * BM * 33 * 4, "partial tiles fit in the stages");
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, 256, smem, s>>>(p);
+  return cudaGetLastError();
+}
+
+template <bool kVec, int BN>
+cudaError_t launch_gemm_f32_tiles(const GemmF32Params& p, int count, cudaStream_t s) {
+  const dim3 grid((p.N + BN - 1) / BN, (p.M + kBM - 1) / kBM, count);
+  auto kern = gemm_f32_kernel<kVec, BN>;
+  constexpr int smem = gemm_f32_smem<BN>();
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, 256, smem, s>>>(p);
+  return cudaGetLastError();
 }
 
 }  // namespace
@@ -340,18 +550,16 @@ cudaError_t launch_sdpa_f32(const SdpaArgs& a, const DeviceCtl& ctl) {
   p.mask_sh = a.mask_sh;
   if (a.Lq == 0 || a.H == 0 || a.B == 0) return cudaSuccess;
   const dim3 grid((a.Lq + kRowsC - 1) / kRowsC, a.H, a.B);
-  auto smem = [](int DP) { return (kRowsC * DP + kKeys * (DP + 1) + kKeys * DP) * 4; };
-  if (a.d <= 32) {
-    sdpa_f32_kernel<32><<<grid, kWarps * 32, smem(32), a.stream>>>(p);
-  } else if (a.d <= 64) {
-    sdpa_f32_kernel<64><<<grid, kWarps * 32, smem(64), a.stream>>>(p);
-  } else {
-    cudaError_t e = cudaFuncSetAttribute(sdpa_f32_kernel<128>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem(128));
+  auto smem = [](int DP) { return (kRowsC * DP + 2 * kKeys * (DP + 1) + 2 * kKeys * DP) * 4; };
+  auto run = [&](auto kern, int DP) -> cudaError_t {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem(DP));
     if (e != cudaSuccess) return e;
-    sdpa_f32_kernel<128><<<grid, kWarps * 32, smem(128), a.stream>>>(p);
-  }
-  return cudaGetLastError();
+    kern<<<grid, kWarps * 32, smem(DP), a.stream>>>(p);
+    return cudaGetLastError();
+  };
+  if (a.d <= 32) return run(sdpa_f32_kernel<32>, 32);
+  if (a.d <= 64) return run(sdpa_f32_kernel<64>, 64);
+  return run(sdpa_f32_kernel<128>, 128);
 }
 
 cudaError_t launch_gemm_f32(const GemmArgs& g, const DeviceCtl&) {
@@ -369,15 +577,22 @@ cudaError_t launch_gemm_f32(const GemmArgs& g, const DeviceCtl&) {
   p.M = g.M;
   p.N = g.N;
   p.K = g.K;
-  const dim3 grid((g.N + kBN - 1) / kBN, (g.M + kBM - 1) / kBM, g.count);
-  if (grid.x == 0 || grid.y == 0) return cudaSuccess;
+  if (g.N <= 0 || g.M <= 0 || g.count <= 0) return cudaSuccess;
   bool vec = g.K % 4 == 0 && g.N % 4 == 0;
   for (int i = 0; i < g.count; ++i)
     vec = vec && (reinterpret_cast<uintptr_t>(p.A[i]) & 15u) == 0 &&
           (reinterpret_cast<uintptr_t>(p.W[i]) & 15u) == 0;
-  if (vec) gemm_f32_kernel<true><<<grid, 256, 0, g.stream>>>(p);
-  else gemm_f32_kernel<false><<<grid, 256, 0, g.stream>>>(p);
-  return cudaGetLastError();
+  // the split-k form when 32 x 64 tiles would not give every SM a CTA
+  int sms = 0, dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return cudaErrorInvalidValue;
+  const long long wide = static_cast<long long>((g.N + 63) / 64) * ((g.M + kBM - 1) / kBM) * g.count;
+  if (wide < sms)
+    return vec ? launch_gemm_f32_splitk<true>(p, g.count, g.stream)
+               : launch_gemm_f32_splitk<false>(p, g.count, g.stream);
+  return vec ? launch_gemm_f32_tiles<true, 64>(p, g.count, g.stream)
+             : launch_gemm_f32_tiles<false, 64>(p, g.count, g.stream);
 }
 
 }  // namespace mha
