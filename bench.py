@@ -350,15 +350,19 @@ def bench_sdpa(args, w, rank, world, local_rank):
     torch.cuda.synchronize()
     with ClockSampler(local_rank) as clocks:
         if flush is None:
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            for _ in range(args.steps):
+            # one event between consecutive steps: the per-step spread comes
+            # from the same timeline as the total
+            evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+            evs[0].record(stream)
+            for i in range(args.steps):
                 step()
-            e1.record(stream)
+                evs[i + 1].record(stream)
             torch.cuda.synchronize()
-            total_ms = e0.elapsed_time(e1)
+            total_ms = evs[0].elapsed_time(evs[-1])
+            step_ms = [evs[i].elapsed_time(evs[i + 1]) for i in range(args.steps)]
         else:
             total_ms = 0.0
+            step_ms = []
             for _ in range(args.steps):
                 flush.zero_()
                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -366,7 +370,19 @@ def bench_sdpa(args, w, rank, world, local_rank):
                 step()
                 e1.record(stream)
                 torch.cuda.synchronize()
-                total_ms += e0.elapsed_time(e1)
+                step_ms.append(e0.elapsed_time(e1))
+                total_ms += step_ms[-1]
+    warm_ms = None
+    if flush is not None:
+        # the same steps back to back, inputs left in L2 (context for the
+        # cold number above, which is the one reported)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        warm_ms = e0.elapsed_time(e1) / args.steps
     barrier()
     torch.cuda.synchronize()
     st = mha.mha_check()
@@ -395,8 +411,15 @@ def bench_sdpa(args, w, rank, world, local_rank):
            "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": out_bytes,
            "ms_per_step": round(e2e_s / e2e_steps * 1e3, 3)}
     del bufs
+    q = sorted(step_ms)
+    pick = lambda f: q[min(len(q) - 1, int(round(f * (len(q) - 1))))]
+    spread = {"median": round(statistics.median(q), 4), "p10": round(pick(0.1), 4),
+              "p90": round(pick(0.9), 4), "unit": "ms"}
+    if warm_ms is not None:
+        spread["warm_l2_ms"] = round(warm_ms, 4)
     return dict(value=value, per_step=per_step, kernel_tflops=kernel_tflops, flops=flops,
                 clocks=clocks.summary(), e2e=e2e, Q=Q, K=K, V=V, lens=lens, dims=dims,
+                step_ms=spread,
                 l2="inputs larger than L2" if flush is None else "L2 flushed between steps")
 
 
@@ -948,6 +971,7 @@ def run_gpu(args):
         "pct_bf16_peak_nominal": round(100.0 * ach / NOMINAL_BF16_TFLOPS, 2),
         "roofline": roofline,
         "e2e": r["e2e"],
+        "step_ms": r["step_ms"],
         "gpu_launches": args.steps,
         "clocks": r["clocks"],
         "cpu_baseline": cpu,
