@@ -35,6 +35,10 @@ Extra legs in the same JSON line:
 Multi-GPU: the path has no exchange step, so N ranks run N replicas (one per
 GPU, weak scaling); the time is the max over ranks after a barrier.
 
+`--workload 1` makes the base-shape multi-head attention layer (B1 L128 D512
+h8, fp32: rows a1-a8 through mha_forward) the step instead, in tokens/s; its
+roofline is the fp32 FMA rate of the CUDA cores.
+
 `--impl reference` times the CPU oracle (the reference arm of this build) on
 the same workload, metric and unit.
 """
@@ -882,6 +886,9 @@ def run_gpu(args):
     if w.kind == "decode":
         run_gpu_decode(args, w, rank, world, local_rank)
         return
+    if w.kind == "mha":
+        run_gpu_mha(args, w, rank, world, local_rank)
+        return
     r = bench_sdpa(args, w, rank, world, local_rank)
     peaks, peak_src = measured_peaks()
 
@@ -986,6 +993,171 @@ def run_gpu(args):
         dist.destroy_process_group()
 
 
+MHA_METRIC = "MHA layer tokens/s"
+
+
+def mha_layer_flops(w) -> float:
+    """Algorithmic flops of one layer: four D x D projections of every token
+    and the attention's two products over every (query, key) pair."""
+    return 4 * 2.0 * w.B * w.Lq * w.D * w.D + 4.0 * w.B * w.H * w.Lq * w.Lk * w.d
+
+
+def oracle_mha_baseline(w, x, Ws, min_seconds=2.0):
+    """The fp64 oracle's layer (as it stands) on the whole input, repeated
+    for about ``min_seconds``: (tokens/s, seconds per layer, threads)."""
+    import oracle
+    orc = oracle.default()
+    n, t0 = 0, time.perf_counter()
+    while True:
+        orc.mha(x, x, *Ws, h=w.H)
+        n += 1
+        dt = time.perf_counter() - t0
+        if dt >= min_seconds:
+            break
+    return w.B * w.Lq * n / dt, dt / n, orc.num_threads()
+
+
+def run_gpu_mha(args, w, rank, world, local_rank):
+    """The base-shape layer as the step: one mha_forward (three launches) per
+    step on device-resident inputs, L2 flushed between steps."""
+    import torch
+    import torch.distributed as dist
+    import transformer_head_scaled_03_gb300 as mha
+    from transformer_head_scaled_03_gb300.inputs import mha_inputs
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    x_h, *Ws_h = mha_inputs(w)
+    tf = lambda a: torch.from_numpy(a)
+    x_pin = tf(x_h).pin_memory()
+    x = x_pin.to(dev)
+    Ws = [tf(W).to(dev) for W in Ws_h]
+    out = torch.empty_like(x)
+    handle = mha.mha_create(w.D, torch.float32, w.B, w.Lq, w.Lk)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        mha.mha_forward(handle, x, x, *Ws, h=w.H, out=out)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert mha.mha_check(handle) == mha.MHA_OK
+    barrier()
+    torch.cuda.synchronize()
+    step_ms = []
+    with ClockSampler(local_rank) as clocks:
+        for _ in range(args.steps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            step()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            step_ms.append(e0.elapsed_time(e1))
+    barrier()
+    torch.cuda.synchronize()
+    st = mha.mha_check(handle)
+    if st != mha.MHA_OK:
+        raise RuntimeError(f"device error during timing: {mha.status_string(st)}")
+    total_ms = sum(step_ms)
+    max_s = max_over_ranks(total_ms / 1e3, dev)
+    tokens = w.B * w.Lq
+    value = whole_job_value(tokens * args.steps, world, max_s)
+    per_step_ms = total_ms / args.steps
+    # context: the same call back to back (inputs in L2) and as a graph replay
+    eager_ms, graph_ms = _time_eager_and_graph(step, 200, 5)
+    # end to end: x from pinned host memory, the layer, out back to the host
+    out_h = torch.empty(x.shape, dtype=torch.float32).pin_memory()
+    torch.cuda.synchronize()
+    barrier()
+    t0 = time.perf_counter()
+    e2e_steps = 50
+    for _ in range(e2e_steps):
+        x.copy_(x_pin, non_blocking=True)
+        step()
+        out_h.copy_(out, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+    e2e_s = max_over_ranks(time.perf_counter() - t0, dev)
+    handle.close()
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+    flops = mha_layer_flops(w)
+    # fp32 FMA rate of the CUDA cores: SMs x 128 lanes x 2 flops x max clock
+    peaks, _ = measured_peaks()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    fma_peak = sms * 128 * 2.0 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
+    achieved = flops / (per_step_ms / 1e3) / 1e12
+    cpu = None
+    if not args.skip_cpu:
+        tps, sec, cores = oracle_mha_baseline(w, x_h, Ws_h)
+        cpu = {"value": round(tps, 2), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+               "seconds_per_layer": round(sec, 4),
+               "sample": "the whole workload (every token of the layer), fp64, repeated for ~2 s"}
+    q = sorted(step_ms)
+    pick = lambda f: q[min(len(q) - 1, int(round(f * (len(q) - 1))))]
+    line = {
+        "metric": MHA_METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(max_s / args.steps * 1e3, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "L": w.Lq, "D": w.D, "h": w.H, "mask": "none",
+                   "flops_per_step": flops, "l2": "L2 flushed between steps",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": {"bound": "alu", "achieved": round(achieved, 3), "peak": round(fma_peak, 2),
+                     "unit": "TFLOP/s", "frac": round(achieved / fma_peak, 4),
+                     "peak_source": f"derived: {sms} SMs x 128 fp32 FMA lanes x 2 flops x "
+                                    f"{peaks.get('sm_max_mhz', 2070.0):.0f} MHz",
+                     "traffic": None,
+                     "kernel": "the layer's three launches (Q/K/V projection, attention, "
+                               "output projection) timed together"},
+        "step_ms": {"median": round(statistics.median(q), 4), "p10": round(pick(0.1), 4),
+                    "p90": round(pick(0.9), 4), "unit": "ms",
+                    "warm_l2_ms": round(eager_ms, 4), "graph_replay_ms": round(graph_ms, 4)},
+        "e2e": {"value": round(whole_job_value(tokens * e2e_steps, world, e2e_s), 1),
+                "unit": "tokens/s", "h2d_bytes_per_step": x.numel() * 4,
+                "d2h_bytes_per_step": out.numel() * 4,
+                "ms_per_step": round(e2e_s / e2e_steps * 1e3, 4)},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clocks.summary(),
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_reference_mha(args, w, world):
+    """The oracle's layer on the whole base-shape input, as the reference arm."""
+    from transformer_head_scaled_03_gb300.inputs import mha_inputs
+    import oracle
+    x, *Ws = mha_inputs(w)
+    orc = oracle.default()
+    for _ in range(args.warmup):
+        orc.mha(x, x, *Ws, h=w.H)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        orc.mha(x, x, *Ws, h=w.H)
+    total_s = time.perf_counter() - t0
+    value = w.B * w.Lq * args.steps / total_s
+    line = {
+        "impl": "reference", "metric": MHA_METRIC, "value": round(value, 2), "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(total_s / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "L": w.Lq, "D": w.D, "h": w.H, "mask": "none"},
+        "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s",
+                         "cores": orc.num_threads(), "kind": "oracle",
+                         "sample": "the whole workload per step, fp64 oracle"},
+        "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
 # ------------------------------------------------------------ reference arm
 
 def run_reference(args):
@@ -998,6 +1170,9 @@ def run_reference(args):
     w = workload_from_args(args)
     if w.kind == "decode":
         run_reference_decode(args, w, world)
+        return
+    if w.kind == "mha":
+        run_reference_mha(args, w, world)
         return
     Q, K, V, lens, _ = sdpa_inputs(w)
     rows = sample_rows(w.B, w.H, w.Lq, args.ref_rows_per_head, seed=w.seed + 4000, must=())
@@ -1072,8 +1247,9 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=60)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
-    ap.add_argument("--workload", type=int, default=5, choices=[2, 3, 4, 5, 6, 7, 8],
-                    help="2-5: attention workloads; 6-8: decode against a cache")
+    ap.add_argument("--workload", type=int, default=5, choices=[1, 2, 3, 4, 5, 6, 7, 8],
+                    help="1: the fp32 base-shape layer; 2-5: attention workloads; "
+                         "6-8: decode against a cache")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the batch size of a decode workload (profiling captures)")
     ap.add_argument("--seq", type=int, default=None,
