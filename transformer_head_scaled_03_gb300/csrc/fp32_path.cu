@@ -19,10 +19,11 @@
 namespace mha {
 namespace {
 
-constexpr int kKeys = 64;   // keys per shared-memory chunk (two per lane)
+constexpr int kKeys = 64;   // keys per shared-memory chunk
 constexpr int kRowsW = 2;   // query rows per warp, processed together
 constexpr int kWarps = 8;   // warps per CTA
-constexpr int kRowsC = kRowsW * kWarps;
+// query rows per CTA with KG key groups (the warps of a group share rows)
+__host__ __device__ constexpr int rows_per_cta(int KG) { return kRowsW * kWarps / KG; }
 
 struct SdpaF32Params {
   const float* Q;
@@ -64,18 +65,24 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-// One CTA = 16 query rows of one (b, h); warp w owns rows 2w, 2w+1 and
-// scores them together against each 64-key chunk (lane j: keys j and j+32),
-// so every K and V element read from shared memory serves two rows.  Eight
-// warps per CTA keep two warps per scheduler busy on the short layers this
-// path serves.  The
-// chunks stream through two shared-memory stages by cp.async: chunk c + 1 is
-// in flight while chunk c is scored, and the first two are requested before
-// Q is read, so the load latencies of a short key range overlap.
+// One CTA = eight warps in KG key groups over 16 / KG query rows of one
+// (b, h).  Warp w of group g owns rows 2w, 2w+1 and scores them together
+// against its keys of each 64-key chunk (KG = 1: lane j takes keys j and
+// j + 32; KG = 2: group g takes keys 32g..32g+31, lane j key 32g + j), so
+// every K and V element read from shared memory serves two rows.  With two
+// groups each keeps its own running max, sum and output and the two are
+// merged at the end: twice the CTAs for a short layer whose 16-row grid
+// would leave SMs idle.  The chunks stream through two shared-memory stages
+// by cp.async: chunk c + 1 is in flight while chunk c is scored, and the
+// first two are requested before Q is read, so the load latencies of a short
+// key range overlap.
 // DP: head-dim bound (d <= DP, DP in {32, 64, 128}).
-template <int DP>
+template <int DP, int KG>
 __global__ void __launch_bounds__(kWarps * 32) sdpa_f32_kernel(const SdpaF32Params p) {
-  constexpr int CPL = DP / 32;  // output columns per lane
+  constexpr int CPL = DP / 32;             // output columns per lane
+  constexpr int KPL = kKeys / 32 / KG;     // keys per lane per chunk
+  constexpr int kGroupWarps = kWarps / KG;
+  constexpr int kRowsC = rows_per_cta(KG);
   extern __shared__ __align__(16) float fsm[];
   float* sQ = fsm;                              // [kRowsC][DP]
   float* sK0 = sQ + kRowsC * DP;                // two stages of [kKeys][DP + 1]
@@ -145,6 +152,9 @@ __global__ void __launch_bounds__(kWarps * 32) sdpa_f32_kernel(const SdpaF32Para
     const int q = row0 + r;
     sQ[idx] = (q < p.Lq && c < d) ? p.Q[(bh * p.Lq + q) * d + c] * p.scale : 0.f;
   }
+  const int grp = warp / kGroupWarps, wg = warp % kGroupWarps;
+  // this lane's keys within a chunk: 32 (grp KPL + t) + lane, t < KPL
+  auto key_of = [&](int t) { return 32 * (grp * KPL + t) + lane; };
   float m[kRowsW], l[kRowsW], o[kRowsW][CPL];
 #pragma unroll
   for (int i = 0; i < kRowsW; ++i) {
@@ -153,64 +163,75 @@ __global__ void __launch_bounds__(kWarps * 32) sdpa_f32_kernel(const SdpaF32Para
 #pragma unroll
     for (int cc = 0; cc < CPL; ++cc) o[i][cc] = 0.f;
   }
-  const float* q_rows = sQ + warp * kRowsW * DP;
+  const float* q_rows = sQ + wg * kRowsW * DP;
   for (int chunk = 0; chunk < n_chunks; ++chunk) {
     const int k0 = chunk * kKeys;
     const float* sK = sK0 + (chunk & 1) * kKeys * (DP + 1);
     const float* sV = sV0 + (chunk & 1) * kKeys * DP;
     cp_async_wait<1>();  // this chunk has landed (the next may be in flight)
     __syncthreads();
-    // scores s[i][t] of row i against key k0 + lane + 32 t (Q pre-scaled)
-    float s[kRowsW][2];
+    // scores s[i][t] of row i against key k0 + key_of(t) (Q pre-scaled)
+    float s[kRowsW][KPL];
 #pragma unroll
-    for (int i = 0; i < kRowsW; ++i) s[i][0] = s[i][1] = 0.f;
-    const float* k_a = sK + lane * (DP + 1);
-    const float* k_b = sK + (lane + 32) * (DP + 1);
+    for (int i = 0; i < kRowsW; ++i)
+#pragma unroll
+      for (int t = 0; t < KPL; ++t) s[i][t] = 0.f;
 #pragma unroll 8
     for (int c = 0; c < DP; ++c) {
-      const float ka = k_a[c], kb = k_b[c];
+      float kv[KPL];
+#pragma unroll
+      for (int t = 0; t < KPL; ++t) kv[t] = sK[key_of(t) * (DP + 1) + c];
 #pragma unroll
       for (int i = 0; i < kRowsW; ++i) {
         const float qv = q_rows[i * DP + c];
-        s[i][0] = fmaf(qv, ka, s[i][0]);
-        s[i][1] = fmaf(qv, kb, s[i][1]);
+#pragma unroll
+        for (int t = 0; t < KPL; ++t) s[i][t] = fmaf(qv, kv[t], s[i][t]);
       }
     }
-    float pj[kRowsW][2];
+    float pj[kRowsW][KPL];
 #pragma unroll
     for (int i = 0; i < kRowsW; ++i) {
-      const int q_row = row0 + warp * kRowsW + i;
+      const int q_row = row0 + wg * kRowsW + i;
+      float mx = -INFINITY;
 #pragma unroll
-      for (int t = 0; t < 2; ++t) {
-        const int key = k0 + lane + 32 * t;
+      for (int t = 0; t < KPL; ++t) {
+        const int key = k0 + key_of(t);
         const bool valid = key < key_end && (!causal || key <= q_row);
         s[i][t] = valid ? s[i][t] : -INFINITY;
         if (p.add_mask && valid && q_row < p.Lq)
           s[i][t] += __ldg(p.add_mask + static_cast<int64_t>(b) * p.mask_sb +
                            static_cast<int64_t>(h) * p.mask_sh +
                            static_cast<int64_t>(q_row) * p.Lk + key);
+        mx = fmaxf(mx, s[i][t]);
       }
-      const float m_new = fmaxf(m[i], warp_max(fmaxf(s[i][0], s[i][1])));
+      const float m_new = fmaxf(m[i], warp_max(mx));
       if (m_new == -INFINITY) {  // nothing visible to this row yet (uniform in the warp)
-        pj[i][0] = pj[i][1] = 0.f;
+#pragma unroll
+        for (int t = 0; t < KPL; ++t) pj[i][t] = 0.f;
         continue;
       }
       const float alpha = expf(m[i] - m_new);
-      pj[i][0] = s[i][0] == -INFINITY ? 0.f : expf(s[i][0] - m_new);
-      pj[i][1] = s[i][1] == -INFINITY ? 0.f : expf(s[i][1] - m_new);
-      l[i] = l[i] * alpha + warp_sum(pj[i][0] + pj[i][1]);
+      float ps = 0.f;
+#pragma unroll
+      for (int t = 0; t < KPL; ++t) {
+        pj[i][t] = s[i][t] == -INFINITY ? 0.f : expf(s[i][t] - m_new);
+        ps += pj[i][t];
+      }
+      l[i] = l[i] * alpha + warp_sum(ps);
 #pragma unroll
       for (int cc = 0; cc < CPL; ++cc) o[i][cc] *= alpha;
       m[i] = m_new;
     }
-    // o[i][c] += sum_j p_ij V[j][c]; lane owns columns lane + 32 cc
+    // o[i][c] += sum_j p_ij V[j][c] over this group's keys; lane owns
+    // columns lane + 32 cc
 #pragma unroll 4
     for (int jj = 0; jj < 32; ++jj) {
 #pragma unroll
-      for (int t = 0; t < 2; ++t) {
+      for (int t = 0; t < KPL; ++t) {
         float vv[CPL];
 #pragma unroll
-        for (int cc = 0; cc < CPL; ++cc) vv[cc] = sV[(jj + 32 * t) * DP + lane + 32 * cc];
+        for (int cc = 0; cc < CPL; ++cc)
+          vv[cc] = sV[(32 * (grp * KPL + t) + jj) * DP + lane + 32 * cc];
 #pragma unroll
         for (int i = 0; i < kRowsW; ++i) {
           const float pv = __shfl_sync(0xffffffffu, pj[i][t], jj);
@@ -224,17 +245,49 @@ __global__ void __launch_bounds__(kWarps * 32) sdpa_f32_kernel(const SdpaF32Para
     cp_async_commit();
   }
   cp_async_wait<0>();
+  float* mrg = sK0;  // [kRowsC][DP + 2]: group 1's max, sum and output rows
+  if constexpr (KG == 2) {
+    // merge the two key groups' partial softmax states through the (now
+    // idle) first K stage
+    __syncthreads();
+    if (grp == 1) {
+#pragma unroll
+      for (int i = 0; i < kRowsW; ++i) {
+        float* row = mrg + (wg * kRowsW + i) * (DP + 2);
+        if (lane == 0) {
+          row[0] = m[i];
+          row[1] = l[i];
+        }
+#pragma unroll
+        for (int cc = 0; cc < CPL; ++cc) row[2 + lane + 32 * cc] = o[i][cc];
+      }
+    }
+    __syncthreads();
+    if (grp != 0) return;
+  }
 #pragma unroll
   for (int i = 0; i < kRowsW; ++i) {
-    const int q_row = row0 + warp * kRowsW + i;
+    const int q_row = row0 + wg * kRowsW + i;
     if (q_row >= p.Lq) continue;
-    const float inv = l[i] > 0.f ? 1.f / l[i] : 0.f;
+    float a0 = 1.f, a1 = 0.f, lsum = l[i];
+    const float* row = mrg + (wg * kRowsW + i) * (DP + 2);
+    if constexpr (KG == 2) {
+      const float m1 = row[0];
+      const float mm = fmaxf(m[i], m1);
+      a0 = m[i] == -INFINITY ? 0.f : expf(m[i] - mm);
+      a1 = m1 == -INFINITY ? 0.f : expf(m1 - mm);
+      lsum = l[i] * a0 + row[1] * a1;
+    }
+    const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
     const size_t row_idx = p.ctx_layout ? (static_cast<size_t>(b) * p.Lq + q_row) * p.H + h
                                         : bh * p.Lq + q_row;
 #pragma unroll
     for (int cc = 0; cc < CPL; ++cc) {
       const int c = lane + 32 * cc;
-      if (c < d) p.O[row_idx * d + c] = o[i][cc] * inv;
+      if (c >= d) continue;
+      float v = o[i][cc] * a0;
+      if constexpr (KG == 2) v += row[2 + c] * a1;
+      p.O[row_idx * d + c] = v * inv;
     }
   }
 }
@@ -549,17 +602,29 @@ cudaError_t launch_sdpa_f32(const SdpaArgs& a, const DeviceCtl& ctl) {
   p.mask_sb = a.mask_sb;
   p.mask_sh = a.mask_sh;
   if (a.Lq == 0 || a.H == 0 || a.B == 0) return cudaSuccess;
-  const dim3 grid((a.Lq + kRowsC - 1) / kRowsC, a.H, a.B);
-  auto smem = [](int DP) { return (kRowsC * DP + 2 * kKeys * (DP + 1) + 2 * kKeys * DP) * 4; };
-  auto run = [&](auto kern, int DP) -> cudaError_t {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem(DP));
+  auto smem = [](int DP, int KG) {
+    return (rows_per_cta(KG) * DP + 2 * kKeys * (DP + 1) + 2 * kKeys * DP) * 4;
+  };
+  auto run = [&](auto kern, int DP, int KG) -> cudaError_t {
+    const int rows = rows_per_cta(KG);
+    const dim3 grid((a.Lq + rows - 1) / rows, a.H, a.B);
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem(DP, KG));
     if (e != cudaSuccess) return e;
-    kern<<<grid, kWarps * 32, smem(DP), a.stream>>>(p);
+    kern<<<grid, kWarps * 32, smem(DP, KG), a.stream>>>(p);
     return cudaGetLastError();
   };
-  if (a.d <= 32) return run(sdpa_f32_kernel<32>, 32);
-  if (a.d <= 64) return run(sdpa_f32_kernel<64>, 64);
-  return run(sdpa_f32_kernel<128>, 128);
+  // two key groups (8-row CTAs) when 16-row CTAs would not give every SM one
+  int sms = 0, dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return cudaErrorInvalidValue;
+  const long long ctas16 =
+      static_cast<long long>((a.Lq + rows_per_cta(1) - 1) / rows_per_cta(1)) * a.H * a.B;
+  const bool split = ctas16 < sms;
+  if (a.d <= 32) return split ? run(sdpa_f32_kernel<32, 2>, 32, 2) : run(sdpa_f32_kernel<32, 1>, 32, 1);
+  if (a.d <= 64) return split ? run(sdpa_f32_kernel<64, 2>, 64, 2) : run(sdpa_f32_kernel<64, 1>, 64, 1);
+  return split ? run(sdpa_f32_kernel<128, 2>, 128, 2) : run(sdpa_f32_kernel<128, 1>, 128, 1);
 }
 
 cudaError_t launch_gemm_f32(const GemmArgs& g, const DeviceCtl&) {
