@@ -13,7 +13,9 @@
 // K-major; W is row-major [K, N], i.e. MN-major for the MMA's B operand, and
 // is loaded as 64 x 64 boxes (64 N-columns of 128 bytes, 64 K-rows).
 // Warp roles: warp 0 TMA producer, warp 1 MMA issuer and TMEM owner,
-// warps 2-5 epilogue (TMEM -> registers -> global, one row per thread).
+// warps 2-5 epilogue (TMEM -> registers, one row per thread; then through
+// a shared-memory transpose so that every store instruction writes whole
+// 128-byte row segments).
 // Up to three problems of one shape share a launch, which is how the Q, K
 // and V projections of self-attention run as one launch.
 //
@@ -47,7 +49,10 @@ constexpr int bDrain = 2 * kStages + 4;
 constexpr int kNumBars = 2 * kStages + 5;
 constexpr int kOffBar = kStages * kStageBytes;
 constexpr int kOffMisc = kOffBar + 8 * kNumBars;
-constexpr int kSmemBytes = kOffMisc + 16 + 1024;
+// epilogue staging: per epilogue warp, 32 rows x 128 bytes (64 bf16 columns)
+constexpr int kOffStage = (kOffMisc + 16 + 127) & ~127;
+constexpr int kStageWarpBytes = 32 * 128;
+constexpr int kSmemBytes = kOffStage + 4 * kStageWarpBytes + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory");
 
 struct GemmParams {
@@ -207,39 +212,82 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int relu = p.relu[z];
       __nv_bfloat16* C = static_cast<__nv_bfloat16*>(p.C[z]);
       const uint32_t tbase = lane_base + static_cast<uint32_t>(b * kBN);
-      for (int cb = 0; cb < kBN / 32; ++cb) {
+      // An element's offset is a row part plus a column part: row-major
+      // m * N + n, or for the head split ((bb * H + hh) * L + l) * dh + c
+      // with m = bb * L + l and n = hh * dh + c.  Each lane computes the row
+      // part of its own row (row `row` of the tile) once per tile.
+      const bool split = store == static_cast<int>(GemmStore::kHeadSplit);
+      long long row_part;
+      if (split) {
+        const int bb = m / L, l = m - bb * L;
+        row_part = (static_cast<long long>(bb) * (p.N / dh) * L + l) * dh;
+      } else {
+        row_part = static_cast<long long>(m) * p.N;
+      }
+      auto col_part = [&](int n) -> long long {
+        if (!split) return n;
+        const int hh = n / dh, c = n - hh * dh;
+        return static_cast<long long>(hh) * L * dh + c;
+      };
+      // bias (bf16) added and ReLU applied to 8 accumulators
+      auto finish8 = [&](uint32_t* v8, int n) -> uint4 {
+        float f[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) f[k] = __uint_as_float(v8[k]);
+        if (bias) {
+          const uint4 bv = __ldg(reinterpret_cast<const uint4*>(bias + n));
+          const __nv_bfloat16* bb = reinterpret_cast<const __nv_bfloat16*>(&bv);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) f[k] += __bfloat162float(bb[k]);
+        }
+        if (relu) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) f[k] = fmaxf(f[k], 0.f);
+        }
+        uint4 w;
+        w.x = pack_bf16x2(f[0], f[1]);
+        w.y = pack_bf16x2(f[2], f[3]);
+        w.z = pack_bf16x2(f[4], f[5]);
+        w.w = pack_bf16x2(f[6], f[7]);
+        return w;
+      };
+      // this warp's staging rows: 32 x 128 bytes, 16-byte piece q of row r at
+      // slot q ^ (r & 7) (conflict-free in both directions)
+      uint4* stg = reinterpret_cast<uint4*>(gbase + kOffStage + (warp - 2) * kStageWarpBytes);
+      int cb = 0;
+      for (; cb + 2 <= kBN / 32 && n0 + cb * 32 + 64 <= p.N; cb += 2) {
+        const int n = n0 + cb * 32;
+        uint32_t v[64];
+        tmem_ld32(tbase + cb * 32, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+        tmem_ld32(tbase + cb * 32 + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+        tmem_ld_wait(v);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) stg[lane * 8 + (q ^ (lane & 7))] = finish8(&v[8 * q], n + 8 * q);
+        __syncwarp();
+        // four rows of 128 bytes per store instruction: lane l takes piece
+        // l % 8 of row 4 i + l / 8
+        const int q = lane & 7;
+        const long long cp = col_part(n + 8 * q);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int rr = 4 * i + (lane >> 3);
+          const uint4 w = stg[rr * 8 + (q ^ (rr & 7))];
+          const long long rp = __shfl_sync(0xffffffffu, row_part, rr);
+          if (m0 + quarter * 32 + rr < p.M) *reinterpret_cast<uint4*>(C + rp + cp) = w;
+        }
+        __syncwarp();  // the staging rows are rewritten by the next pair
+      }
+      // a trailing 32-column block (N not a multiple of 64): row by row
+      for (; cb < kBN / 32; ++cb) {
         const int n = n0 + cb * 32;
         if (n >= p.N) break;  // uniform across the warp
         uint32_t v[32];
         tmem_ld32(tbase + cb * 32, v);
         tmem_ld_wait(v);
-        if (bias) {
-#pragma unroll
-          for (int k = 0; k < 32; ++k)
-            v[k] = __float_as_uint(__uint_as_float(v[k]) + __bfloat162float(bias[n + k]));
-        }
-        if (relu) {
-#pragma unroll
-          for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(fmaxf(__uint_as_float(v[k]), 0.f));
-        }
         if (m < p.M) {
-          size_t off;
-          if (store == static_cast<int>(GemmStore::kHeadSplit)) {
-            const int bb = m / L, l = m - bb * L, hh = n / dh, c = n - hh * dh;
-            off = ((static_cast<size_t>(bb) * (p.N / dh) + hh) * L + l) * dh + c;
-          } else {
-            off = static_cast<size_t>(m) * p.N + n;
-          }
-          uint4* dst = reinterpret_cast<uint4*>(C + off);
+          uint4* dst = reinterpret_cast<uint4*>(C + row_part + col_part(n));
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(v[8 * k + 0]), __uint_as_float(v[8 * k + 1]));
-            w.y = pack_bf16x2(__uint_as_float(v[8 * k + 2]), __uint_as_float(v[8 * k + 3]));
-            w.z = pack_bf16x2(__uint_as_float(v[8 * k + 4]), __uint_as_float(v[8 * k + 5]));
-            w.w = pack_bf16x2(__uint_as_float(v[8 * k + 6]), __uint_as_float(v[8 * k + 7]));
-            dst[k] = w;
-          }
+          for (int k = 0; k < 4; ++k) dst[k] = finish8(&v[8 * k], n + 8 * k);
         }
       }
       // this accumulator may take the tile after next
