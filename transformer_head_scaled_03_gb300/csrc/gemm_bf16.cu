@@ -236,9 +236,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int k = 0; k < 8; ++k) f[k] = __uint_as_float(v8[k]);
         if (bias) {
           const uint4 bv = __ldg(reinterpret_cast<const uint4*>(bias + n));
-          const __nv_bfloat16* bb = reinterpret_cast<const __nv_bfloat16*>(&bv);
+          const __nv_bfloat16* b8 = reinterpret_cast<const __nv_bfloat16*>(&bv);
 #pragma unroll
-          for (int k = 0; k < 8; ++k) f[k] += __bfloat162float(bb[k]);
+          for (int k = 0; k < 8; ++k) f[k] += __bfloat162float(b8[k]);
         }
         if (relu) {
 #pragma unroll
@@ -252,7 +252,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         return w;
       };
       // this warp's staging rows: 32 x 128 bytes, 16-byte piece q of row r at
-      // slot q ^ (r & 7) (conflict-free in both directions)
+      // slot q ^ (r & 7), so that both the row-wise writes and the
+      // piece-wise reads take the minimum four 128-byte wavefronts
       uint4* stg = reinterpret_cast<uint4*>(gbase + kOffStage + (warp - 2) * kStageWarpBytes);
       int cb = 0;
       for (; cb + 2 <= kBN / 32 && n0 + cb * 32 + 64 <= p.N; cb += 2) {
@@ -265,12 +266,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int q = 0; q < 8; ++q) stg[lane * 8 + (q ^ (lane & 7))] = finish8(&v[8 * q], n + 8 * q);
         __syncwarp();
         // four rows of 128 bytes per store instruction: lane l takes piece
-        // l % 8 of row 4 i + l / 8
+        // l % 8 of row 4 g4 + l / 8
         const int q = lane & 7;
         const long long cp = col_part(n + 8 * q);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int rr = 4 * i + (lane >> 3);
+        for (int g4 = 0; g4 < 8; ++g4) {
+          const int rr = 4 * g4 + (lane >> 3);
           const uint4 w = stg[rr * 8 + (q ^ (rr & 7))];
           const long long rp = __shfl_sync(0xffffffffu, row_part, rr);
           if (m0 + quarter * 32 + rr < p.M) *reinterpret_cast<uint4*>(C + rp + cp) = w;
