@@ -459,8 +459,52 @@ __global__ void __launch_bounds__(Cfg<D, NQT, NST, BN>::kThreads, Cfg<D, NQT, NS
     const size_t row_idx = p.ctx_layout
                                ? (static_cast<size_t>(b) * p.Lq + q_row) * p.H + h
                                : static_cast<size_t>(bh) * p.Lq + q_row;
+    bool stored = false;
+    if constexpr (D == 64) {
+      if (!p.out_f32) {
+        // A bf16 row of d = 64 is 128 bytes.  The warp's 32 rows go through
+        // shared memory (this tile's Q block, free once bO covered its last
+        // Q K^T product) so that each store writes four whole rows: 16-byte
+        // piece q of row r at slot q ^ (r & 7).
+        uint32_t o[64];
+        if (have) {
+          tmem_ld32(tO, *reinterpret_cast<uint32_t(*)[32]>(&o[0]));
+          tmem_ld32(tO + 32, *reinterpret_cast<uint32_t(*)[32]>(&o[32]));
+          tmem_ld_wait(o);
+        } else {
 #pragma unroll
-    for (int cb = 0; cb < D / 32; ++cb) {
+          for (int i = 0; i < 64; ++i) o[i] = 0u;
+        }
+        uint4* stg = reinterpret_cast<uint4*>(gbase + C::kOffQ + t * C::kQTileBytes +
+                                              quarter * (32 * 128));
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          uint4 v;
+          v.x = pack_bf16x2(__uint_as_float(o[8 * q + 0]) * inv_l,
+                            __uint_as_float(o[8 * q + 1]) * inv_l);
+          v.y = pack_bf16x2(__uint_as_float(o[8 * q + 2]) * inv_l,
+                            __uint_as_float(o[8 * q + 3]) * inv_l);
+          v.z = pack_bf16x2(__uint_as_float(o[8 * q + 4]) * inv_l,
+                            __uint_as_float(o[8 * q + 5]) * inv_l);
+          v.w = pack_bf16x2(__uint_as_float(o[8 * q + 6]) * inv_l,
+                            __uint_as_float(o[8 * q + 7]) * inv_l);
+          stg[lane * 8 + (q ^ (lane & 7))] = v;
+        }
+        __syncwarp();
+        const int q = lane & 7;
+#pragma unroll
+        for (int g4 = 0; g4 < 8; ++g4) {
+          const int rr = 4 * g4 + (lane >> 3);  // the warp's row rr, lane rr's own row
+          const uint4 w = stg[rr * 8 + (q ^ (rr & 7))];
+          const unsigned long long ri = __shfl_sync(0xffffffffu, static_cast<unsigned long long>(row_idx), rr);
+          if (q0 + t * kBlockM + quarter * 32 + rr < p.Lq)
+            reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.O) + ri * D)[q] = w;
+        }
+        stored = true;
+      }
+    }
+#pragma unroll
+    for (int cb = 0; cb < D / 32 && !stored; ++cb) {
       uint32_t o[32];
       if (have) {
         tmem_ld32(tO + cb * 32, o);
