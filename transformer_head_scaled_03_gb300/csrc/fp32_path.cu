@@ -1,9 +1,11 @@
 // fp32_path.cu -- fp32 CUDA-core kernels for callers that need fp32
 // accuracy (max |err| ~1e-6 against an fp64 reference, where bf16 or TF32
 // tensor-core inputs would not do):
-//   * scaled dot-product attention, one warp per two query rows, lane j
-//     scoring keys j and j + 32 of a 64-key chunk held in shared memory, the
-//     row max and row sum reduced with warp shuffles, online over the chunks;
+//   * scaled dot-product attention, one warp per two query rows against
+//     64-key chunks held in shared memory (lane j scoring keys j and j + 32,
+//     or, for short layers, two key groups of warps with lane j scoring key
+//     32g + j and a final merge), the row max and row sum reduced with warp
+//     shuffles, online over the chunks;
 //   * a tiled GEMM C = A @ W with the head-split or row-major store (32 x 64
 //     tiles, or 16 x 32 tiles with the k-steps split inside the CTA for
 //     problems too small to fill the GPU).
