@@ -301,6 +301,22 @@ def workload_from_args(args):
 
 # ------------------------------------------------------------------ GPU arm
 
+def attention_roofline(flops, alg_bytes, achieved_tflops, bf16_peak_tflops, hbm_peak_gbs,
+                       peak_src):
+    """The roofline object of an attention launch: the bound is whichever
+    peak the workload's arithmetic intensity meets first -- tensor at or
+    above the ridge (peak flop/s over peak B/s), HBM below it, where the same
+    time is reported as algorithmic GB/s."""
+    if flops / alg_bytes >= bf16_peak_tflops * 1e12 / (hbm_peak_gbs * 1e9):
+        return {"bound": "tensor", "achieved": round(achieved_tflops, 2),
+                "peak": bf16_peak_tflops, "unit": "TFLOP/s",
+                "frac": round(achieved_tflops / bf16_peak_tflops, 4),
+                "peak_source": f"{peak_src} bf16 burst"}
+    gbs = alg_bytes / (flops / (achieved_tflops * 1e12)) / 1e9
+    return {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak_gbs, "unit": "GB/s",
+            "frac": round(gbs / hbm_peak_gbs, 4), "peak_source": f"{peak_src} HBM copy"}
+
+
 def fwd_kernel_name(w):
     """The forward instantiation sdpa_forward picks for workload w:
     <head dim, query tiles per CTA, K/V stages, keys per tile>."""
@@ -943,18 +959,8 @@ def run_gpu(args):
         traffic = recorded_traffic(["transformer_head_scaled_03_gb300/csrc/sdpa_bf16.cu",
                                     "transformer_head_scaled_03_gb300/csrc/ptx.cuh"],
                                    "profiles/sdpa_fwd_bf16_long_context.md")
-    # the bound is whichever peak the workload's arithmetic intensity meets
-    # first: tensor above the ridge (peak flop/s / peak B/s), HBM below it
     alg_bytes = w.sdpa_bytes(r["lens"])
-    if r["flops"] / alg_bytes >= peak * 1e12 / (peaks["hbm_gbs"] * 1e9):
-        roofline = {"bound": "tensor", "achieved": round(ach, 2), "peak": peak,
-                    "unit": "TFLOP/s", "frac": round(ach / peak, 4),
-                    "peak_source": f"{peak_src} bf16 burst"}
-    else:
-        gbs = alg_bytes / (r["flops"] / (ach * 1e12)) / 1e9
-        roofline = {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
-                    "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
-                    "peak_source": f"{peak_src} HBM copy"}
+    roofline = attention_roofline(r["flops"], alg_bytes, ach, peak, peaks["hbm_gbs"], peak_src)
     roofline.update({"traffic": traffic, "algorithmic_bytes": int(alg_bytes),
                      "kernel": fwd_kernel_name(w)})
     line = {
