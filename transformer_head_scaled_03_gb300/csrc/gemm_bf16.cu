@@ -303,17 +303,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc<kTmemCols>(tmem);
 }
 
+// SMs of the current device, asked at every launch (the runtime answers from
+// its cached device properties), so that each device gets its own count; 1
+// if the query fails, which only shrinks the grid.
 int num_sms() {
-  static int n = 0;
-  if (n <= 0) {
-    int dev = 0, v = 0;
-    if (cudaGetDevice(&dev) == cudaSuccess &&
-        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0)
-      n = v;
-    else
-      n = 148;
-  }
-  return n;
+  int dev = 0, v = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess &&
+      cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0)
+    return v;
+  return 1;
 }
 
 }  // namespace
