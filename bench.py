@@ -13,6 +13,12 @@ Extra legs in the same JSON line:
                attention chunk by chunk): H2D of Q/K/V and D2H of O inside the
                timed region
   roofline     the fused kernel against the measured bf16 tensor peak
+  workloads    the other workloads, each with its own roofline: the
+               key-padding encoder, decoder causal and cross-attention
+               attention workloads (median of per-step CUDA events, L2
+               flushed before each step unless the inputs exceed L2), and the
+               base-shape fp32 layer in tokens/s with the oracle's layer on
+               the host beside it (all threads and one thread)
   mha_layer    the whole layer (rows a1-a8: projections with head-split
                stores, attention with the concat store, output projection)
                in tokens/s, on the same shape (D = 4096, h = 32) and on the
@@ -31,6 +37,8 @@ Extra legs in the same JSON line:
   backward     sdpa_backward (dQ, dK, dV) on the long-context and decoder
                causal shapes, in TFLOP/s (2.5x the forward's flops)
   cpu_baseline the fp64 oracle on this host's cores on a bounded row sample
+               (the same sample every step of the reference arm times), with
+               the full-output time extrapolated from it
 
 Multi-GPU: the path has no exchange step, so N ranks run N replicas (one per
 GPU, weak scaling); the time is the max over ranks after a barrier.
@@ -261,6 +269,24 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sms), "source": "nvidia-smi, 20 ms"}
 
 
+# query rows per head of the oracle's sample, per attention workload: about
+# 5 s of fp64 work on a 16-core host.  The CPU-baseline leg of the GPU arm
+# and every step of the reference arm time this same sample.
+ORACLE_ROWS_PER_HEAD = {2: 48, 3: 256, 4: 96, 5: 512}
+
+
+def oracle_sample(w, per_head=None):
+    """(rows, per_head): the seeded query-row sample the oracle is timed on."""
+    from transformer_head_scaled_03_gb300.inputs import sample_rows
+    n = min(per_head or ORACLE_ROWS_PER_HEAD.get(w.wid, 64), w.Lq)
+    return sample_rows(w.B, w.H, w.Lq, n, seed=w.seed + 3000, must=()), n
+
+
+def sample_description(w, rows, per_head):
+    return (f"{rows.size} query rows ({per_head} per head, all {w.B * w.H} heads, seeded) "
+            f"of the same workload, fp64")
+
+
 def oracle_cpu_baseline(w, Q, K, V, lens, rows):
     """Time the fp64 oracle (as it stands) on a row sample; TFLOP/s."""
     import oracle
@@ -311,10 +337,33 @@ def attention_roofline(flops, alg_bytes, achieved_tflops, bf16_peak_tflops, hbm_
         return {"bound": "tensor", "achieved": round(achieved_tflops, 2),
                 "peak": bf16_peak_tflops, "unit": "TFLOP/s",
                 "frac": round(achieved_tflops / bf16_peak_tflops, 4),
+                "frac_nominal": round(achieved_tflops / NOMINAL_BF16_TFLOPS, 4),
                 "peak_source": f"{peak_src} bf16 burst"}
     gbs = alg_bytes / (flops / (achieved_tflops * 1e12)) / 1e9
     return {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak_gbs, "unit": "GB/s",
-            "frac": round(gbs / hbm_peak_gbs, 4), "peak_source": f"{peak_src} HBM copy"}
+            "frac": round(gbs / hbm_peak_gbs, 4),
+            "frac_nominal": round(gbs / NOMINAL_HBM_GBS, 4),
+            "peak_source": f"{peak_src} HBM copy"}
+
+
+MASK_NAMES = {0: "none", 1: "causal", 2: "key_padding", 3: "causal+key_padding"}
+
+
+def sdpa_l2_note(w) -> str:
+    """How the timed steps treat L2 for workload w: its inputs and output
+    (bf16) larger than two L2s stream from HBM anyway; smaller ones get a
+    256 MB write between steps."""
+    nbytes = 2 * w.H * w.d * (2 * w.B * w.Lq + 2 * w.B * w.Lk)
+    return "inputs larger than L2" if nbytes >= 2 * L2_BYTES else "L2 flushed between steps"
+
+
+def sdpa_config(w, lens, world, float_mask=False):
+    """The `config` object of an attention workload's JSON line (both arms)."""
+    return {"workload": w.name, "B": w.B, "H": w.H, "Lq": w.Lq, "Lk": w.Lk, "d": w.d,
+            "mask": MASK_NAMES[w.mask] + (" (as additive float mask [Lq, Lk])" if float_mask
+                                          else ""),
+            "flops_per_step": w.flops(lens), "l2": sdpa_l2_note(w),
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
 
 
 def fwd_kernel_name(w):
@@ -345,7 +394,7 @@ def bench_sdpa(args, w, rank, world, local_rank):
     in_bytes = sum(t.numel() * t.element_size() for t in (Qd, Kd, Vd))
     out_bytes = Od.numel() * Od.element_size()
     flush = None
-    if in_bytes + out_bytes < 2 * L2_BYTES:
+    if sdpa_l2_note(w) != "inputs larger than L2":
         flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
 
     add_mask = None
@@ -441,6 +490,146 @@ def bench_sdpa(args, w, rank, world, local_rank):
                 clocks=clocks.summary(), e2e=e2e, Q=Q, K=K, V=V, lens=lens, dims=dims,
                 step_ms=spread,
                 l2="inputs larger than L2" if flush is None else "L2 flushed between steps")
+
+
+def _cold_steps(step, steps, flush):
+    """Per-step device times (ms) of ``steps`` calls of ``step`` on the
+    current stream: one event between consecutive steps when ``flush`` is
+    None (inputs larger than L2), else a 256 MB write before each step and
+    each step timed by its own event pair."""
+    import torch
+    stream = torch.cuda.current_stream()
+    if flush is None:
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+        evs[0].record(stream)
+        for i in range(steps):
+            step()
+            evs[i + 1].record(stream)
+        torch.cuda.synchronize()
+        return [evs[i].elapsed_time(evs[i + 1]) for i in range(steps)]
+    out = []
+    for _ in range(steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        out.append(e0.elapsed_time(e1))
+    return out
+
+
+def bench_attention_workload(w, steps, warmup, local_rank, peaks, peak_src):
+    """One attention workload (the inputs the parity tests use), cold L2:
+    median step time, achieved TFLOP/s or GB/s against its roofline."""
+    import torch
+    import transformer_head_scaled_03_gb300 as mha
+    from transformer_head_scaled_03_gb300.inputs import sdpa_inputs
+
+    dev = torch.device("cuda", local_rank)
+    Q, K, V, lens, _ = sdpa_inputs(w)
+    mk = lambda a: torch.from_numpy(a).to(torch.bfloat16).to(dev)
+    Qd, Kd, Vd = mk(Q), mk(K), mk(V)
+    del Q, K, V
+    kl = torch.from_numpy(lens).to(dev) if lens is not None else None
+    Od = torch.empty_like(Qd)
+    l2 = sdpa_l2_note(w)
+    flush = (None if l2 == "inputs larger than L2"
+             else torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev))
+
+    def step():
+        mha.sdpa_forward(Qd, Kd, Vd, mask_kind=w.mask, key_lengths=kl, out=Od)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    st = mha.mha_check()
+    if st != mha.MHA_OK:
+        raise RuntimeError(mha.status_string(st))
+    ms = _cold_steps(step, steps, flush)
+    st = mha.mha_check()
+    if st != mha.MHA_OK:
+        raise RuntimeError(mha.status_string(st))
+    med = statistics.median(ms)
+    flops, nbytes = w.flops(lens), w.sdpa_bytes(lens)
+    tflops = flops / (med / 1e3) / 1e12
+    roof = attention_roofline(flops, nbytes, tflops, peaks["bf16_tflops"], peaks["hbm_gbs"],
+                              peak_src)
+    roof.update({"algorithmic_bytes": int(nbytes), "kernel": fwd_kernel_name(w)})
+    del Qd, Kd, Vd, Od, flush
+    torch.cuda.empty_cache()
+    return {"workload": w.name, "wid": w.wid, "mask": MASK_NAMES[w.mask],
+            "us_per_step": round(med * 1e3, 2), "us_p10": round(sorted(ms)[len(ms) // 10] * 1e3, 2),
+            "tflops": round(tflops, 2), "pct_bf16_peak_nominal": round(100 * tflops / NOMINAL_BF16_TFLOPS, 2),
+            "flops_per_step": flops, "roofline": roof, "l2": l2, "steps": steps,
+            "timing": "median of per-step CUDA events on the launching stream",
+            "gpu_launches_per_step": 1}
+
+
+def bench_base_layer_cold(steps, warmup, local_rank, peaks):
+    """The base-shape layer (workload 1: B1 L128 D512 h8 fp32, mha_forward,
+    three launches) with L2 flushed before every step: median tokens/s, and
+    the oracle's layer on the host with all threads and with one."""
+    import torch
+    import transformer_head_scaled_03_gb300 as mha
+    from transformer_head_scaled_03_gb300.inputs import WORKLOADS, mha_inputs
+
+    w = WORKLOADS[1]
+    dev = torch.device("cuda", local_rank)
+    x_h, *Ws_h = mha_inputs(w)
+    x = torch.from_numpy(x_h).to(dev)
+    Ws = [torch.from_numpy(W).to(dev) for W in Ws_h]
+    out = torch.empty_like(x)
+    handle = mha.mha_create(w.D, torch.float32, w.B, w.Lq, w.Lk)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    try:
+        step = lambda: mha.mha_forward(handle, x, x, *Ws, h=w.H, out=out)
+        for _ in range(warmup):
+            step()
+        torch.cuda.synchronize()
+        ms = _cold_steps(step, steps, flush)
+        st = mha.mha_check(handle)
+        if st != mha.MHA_OK:
+            raise RuntimeError(mha.status_string(st))
+    finally:
+        handle.close()
+    med = statistics.median(ms)
+    flops = mha_layer_flops(w)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    fma_peak = sms * 128 * 2.0 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
+    achieved = flops / (med / 1e3) / 1e12
+    return {"workload": w.name, "wid": 1, "mask": "none",
+            "us_per_step": round(med * 1e3, 2), "tokens_per_s": round(w.B * w.Lq / (med / 1e3), 1),
+            "flops_per_step": flops,
+            "roofline": {"bound": "alu", "achieved": round(achieved, 3), "peak": round(fma_peak, 2),
+                         "unit": "TFLOP/s", "frac": round(achieved / fma_peak, 4),
+                         "peak_source": "derived: SMs x 128 fp32 FMA lanes x 2 flops x max clock",
+                         "kernel": "the layer's launches timed together"},
+            "l2": "L2 flushed between steps", "steps": steps,
+            "timing": "median of per-step CUDA events on the launching stream",
+            "gpu_launches_per_step": 3}
+
+
+def oracle_base_layer(n_threads_list=(0, 1), min_seconds=1.0):
+    """The oracle's base-shape layer on the host: tokens/s with all threads
+    (0) and with one."""
+    from transformer_head_scaled_03_gb300.inputs import WORKLOADS, mha_inputs
+    import oracle
+    w = WORKLOADS[1]
+    x, *Ws = mha_inputs(w)
+    orc = oracle.default()
+    res = {}
+    for nt in n_threads_list:
+        orc.mha(x, x, *Ws, h=w.H, nthreads=nt)
+        n, t0 = 0, time.perf_counter()
+        while True:
+            orc.mha(x, x, *Ws, h=w.H, nthreads=nt)
+            n += 1
+            dt = time.perf_counter() - t0
+            if dt >= min_seconds:
+                break
+        res[nt] = (w.B * w.Lq * n / dt, dt / n)
+    return res, orc.num_threads()
 
 
 def bench_mha_layer(w_shape, dtype_name, steps, warmup, local_rank, seed_w=None):
@@ -580,6 +769,7 @@ def bench_decode(w, steps, warmup, local_rank, hbm_peak):
     return {"workload": w.name, "Lq": w.Lq, "splits": splits,
             "us_per_call": round(ms * 1e3, 2),
             "GB_per_s": round(gbs, 1), "hbm_frac": round(gbs / hbm_peak, 4),
+            "hbm_frac_nominal": round(gbs / NOMINAL_HBM_GBS, 4),
             "bytes_per_call": int(nbytes),
             "tflops": round(w.flops(lens) / (ms / 1e3) / 1e12, 2),
             "tokens_per_s": round(w.B * w.Lq / (ms / 1e3), 1),
@@ -743,6 +933,7 @@ def run_gpu_decode(args, w, rank, world, local_rank):
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": {"bound": "hbm", "achieved": round(kernel_gbs, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(kernel_gbs / peak, 4),
+                     "frac_nominal": round(kernel_gbs / NOMINAL_HBM_GBS, 4),
                      "peak_source": f"{peak_src} HBM copy", "traffic": traffic,
                      "kernel": f"sdpa_decode_bf16_kernel<{w.d}>"},
         "tflops": round(w.flops(lens) / (total_ms / 1e3 / args.steps) / 1e12, 2),
@@ -779,6 +970,7 @@ def bench_embed_pe(shape, steps, warmup, local_rank, hbm_peak, layer_shape=None)
     out = {"shape": {"B": B, "L": L, "D": D, "vocab": vocab, "dtype": "bf16"},
            "us_per_call": round(graph_ms * 1e3, 2), "GB_per_s": round(nbytes / graph_ms / 1e6, 1),
            "hbm_frac": round(nbytes / graph_ms / 1e6 / hbm_peak, 4),
+           "hbm_frac_nominal": round(nbytes / graph_ms / 1e6 / NOMINAL_HBM_GBS, 4),
            "bytes_per_call": nbytes, "tokens_per_s": round(rows / (graph_ms / 1e3), 1),
            "timing": "CUDA graph replay", "gpu_launches_per_call": 1}
     if layer_shape is not None:
@@ -908,6 +1100,21 @@ def run_gpu(args):
     r = bench_sdpa(args, w, rank, world, local_rank)
     peaks, peak_src = measured_peaks()
 
+    workloads = None
+    if not args.skip_workloads:
+        workloads = [bench_attention_workload(WORKLOADS[i], 20, 3, local_rank, peaks, peak_src)
+                     for i in (2, 3, 4)]
+        base = bench_base_layer_cold(50, 5, local_rank, peaks)
+        if rank == 0 and not args.skip_cpu:
+            res, cores = oracle_base_layer()
+            base["cpu_baseline"] = {
+                "value": round(res[0][0], 1), "unit": "tokens/s", "cores": cores,
+                "kind": "oracle", "seconds_per_layer": round(res[0][1], 4),
+                "one_thread": {"value": round(res[1][0], 1), "unit": "tokens/s", "cores": 1,
+                               "seconds_per_layer": round(res[1][1], 4)},
+                "sample": "the whole layer (every token), fp64, repeated for ~1 s"}
+        workloads.insert(0, base)
+
     mha_layer = None
     if not args.skip_mha:
         mha_layer = [bench_mha_layer((w.B, w.Lq, w.H * w.d, w.H), "bf16", 3, 3, local_rank),
@@ -939,14 +1146,17 @@ def run_gpu(args):
 
     cpu = None
     if rank == 0 and not args.skip_cpu:
-        # about 10 s of fp64 oracle work on a 16-core host
-        per_head = args.cpu_rows_per_head or {2: 48, 3: 256, 4: 96, 5: 512}[args.workload]
-        rows = sample_rows(w.B, w.H, w.Lq, min(per_head, w.Lq), seed=w.seed + 3000, must=())
+        # the sample the reference arm times at every step
+        rows, per_head = oracle_sample(w, args.cpu_rows_per_head)
         tf, dt, cores = oracle_cpu_baseline(w, r["Q"], r["K"], r["V"], r["lens"], rows)
         cpu = {"value": round(tf, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-               "seconds": round(dt, 2),
-               "sample": f"{rows.size} query rows ({min(per_head, w.Lq)} per head, all "
-                         f"{w.B * w.H} heads, seeded) of the same workload, fp64"}
+               "seconds": round(dt, 2), "sample": sample_description(w, rows, per_head)}
+        if rows.size < w.B * w.H * w.Lq:
+            # every output row at the sample's rate: the oracle's cost per row
+            # is proportional to the keys the row sees, i.e. to its flops
+            cpu["extrapolated_full_output_seconds"] = round(r["flops"] / (tf * 1e12), 1)
+            cpu["extrapolation"] = ("extrapolated, not measured: the workload's algorithmic "
+                                    "flops over the sample's measured oracle rate")
 
     if rank != 0:
         if world > 1:
@@ -976,11 +1186,7 @@ def run_gpu(args):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": w.name, "B": w.B, "H": w.H, "Lq": w.Lq, "Lk": w.Lk, "d": w.d,
-                   "mask": ({0: "none", 1: "causal", 2: "key_padding", 3: "causal+key_padding"}[w.mask]
-                            + (" (as additive float mask [Lq, Lk])" if args.float_mask else "")),
-                   "flops_per_step": w.flops(r["lens"]), "l2": r["l2"],
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "config": sdpa_config(w, r["lens"], world, args.float_mask),
         "pct_bf16_peak_nominal": round(100.0 * ach / NOMINAL_BF16_TFLOPS, 2),
         "roofline": roofline,
         "e2e": r["e2e"],
@@ -988,6 +1194,7 @@ def run_gpu(args):
         "gpu_launches": args.steps,
         "clocks": r["clocks"],
         "cpu_baseline": cpu,
+        "workloads": workloads,
         "mha_layer": mha_layer,
         "encoder_layer": encoder_layer,
         "embed_pe": embed,
@@ -1181,7 +1388,7 @@ def run_reference(args):
         run_reference_mha(args, w, world)
         return
     Q, K, V, lens, _ = sdpa_inputs(w)
-    rows = sample_rows(w.B, w.H, w.Lq, args.ref_rows_per_head, seed=w.seed + 4000, must=())
+    rows, per_head = oracle_sample(w, args.cpu_rows_per_head)
     for _ in range(args.warmup):
         oracle_cpu_baseline(w, Q, K, V, lens, rows[: max(1, rows.size // 8)])
     total_s, total_flops = 0.0, 0.0
@@ -1191,14 +1398,14 @@ def run_reference(args):
         total_s += dt
         total_flops += tf * 1e12 * dt
     value = total_flops / total_s / 1e12
-    sample = (f"{rows.size} query rows per step ({args.ref_rows_per_head} per head, all "
-              f"{w.B * w.H} heads, seeded) of the workload, fp64 oracle")
+    sample = (f"per step, {sample_description(w, rows, per_head)} oracle (the CPU-baseline "
+              f"leg's sample)")
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(total_s / args.steps * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "B": w.B, "H": w.H, "Lq": w.Lq, "Lk": w.Lk, "d": w.d},
+        "config": sdpa_config(w, lens, world, args.float_mask),
         "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores,
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -1268,9 +1475,11 @@ def main(argv=None):
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--skip-decode", action="store_true")
     ap.add_argument("--skip-backward", action="store_true")
+    ap.add_argument("--skip-workloads", action="store_true",
+                    help="leave out the per-workload legs (workloads 1-4) of the default line")
     ap.add_argument("--cpu-rows-per-head", type=int, default=None,
-                    help="oracle CPU-baseline sample (default: about 10 s of work)")
-    ap.add_argument("--ref-rows-per-head", type=int, default=4)
+                    help="query rows per head of the oracle's sample, for the CPU-baseline "
+                         "leg and each reference-arm step (default: about 5 s of work)")
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per launch of the fused kernel from an ncu capture")
     args = ap.parse_args(argv)

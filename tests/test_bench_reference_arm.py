@@ -54,3 +54,19 @@ def test_reference_arm_two_ranks_prints_once():
     lines = _lines(r.stdout)
     assert len(lines) == 1
     _check(lines[0], 2)
+
+
+def test_reference_arm_attention_workload_config_matches_gpu_arm():
+    """On an attention workload the reference arm's config is the object the
+    GPU arm prints (mask, flops, L2 treatment included)."""
+    import bench
+    from transformer_head_scaled_03_gb300.inputs import WORKLOADS, sdpa_inputs
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload", "2",
+                        "--steps", "1", "--warmup", "3", "--cpu-rows-per-head", "2"],
+                       cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr
+    lines = _lines(r.stdout)
+    assert len(lines) == 1
+    w = WORKLOADS[2]
+    assert lines[0]["config"] == json.loads(json.dumps(bench.sdpa_config(w, sdpa_inputs(w)[3], 1)))
+    assert lines[0]["unit"] == "TFLOP/s" and lines[0]["value"] > 0

@@ -38,3 +38,31 @@ def test_hbm_bound_reports_the_same_time_in_bytes():
     assert r["frac"] == pytest.approx(1000.0 / PEAK_GBS, abs=1e-4)
     r = bench.attention_roofline(1e12, 1e7, 100.0, PEAK_TF, PEAK_GBS, "measured")
     assert r["bound"] == "tensor" and r["frac"] == pytest.approx(100.0 / PEAK_TF, abs=1e-4)
+
+
+def test_nominal_fraction_beside_the_measured_one():
+    r = bench.attention_roofline(1e9, 1e7, 100.0, PEAK_TF, PEAK_GBS, "measured")
+    assert r["frac_nominal"] == pytest.approx(1000.0 / bench.NOMINAL_HBM_GBS, abs=1e-4)
+    r = bench.attention_roofline(1e12, 1e7, 100.0, PEAK_TF, PEAK_GBS, "measured")
+    assert r["frac_nominal"] == pytest.approx(100.0 / bench.NOMINAL_BF16_TFLOPS, abs=1e-4)
+
+
+@pytest.mark.parametrize("wid", [2, 3, 4, 5])
+def test_one_oracle_sample_per_workload(wid):
+    """The CPU-baseline leg and the reference arm time the same rows."""
+    w = WORKLOADS[wid]
+    a, na = bench.oracle_sample(w)
+    b, nb = bench.oracle_sample(w)
+    assert na == nb and np.array_equal(a, b)
+    assert a.size == w.B * w.H * na
+    assert np.all((a >= 0) & (a < w.B * w.H * w.Lq))
+
+
+def test_config_names_the_mask_and_l2_treatment():
+    lens = sdpa_inputs(WORKLOADS[2])[3]
+    c = bench.sdpa_config(WORKLOADS[2], lens, 1)
+    assert c["mask"] == "key_padding" and c["l2"] == "L2 flushed between steps"
+    c = bench.sdpa_config(WORKLOADS[5], None, 1)
+    assert c["mask"] == "causal" and c["l2"] == "inputs larger than L2"
+    assert bench.sdpa_config(WORKLOADS[4], None, 1)["l2"] == "L2 flushed between steps"
+    assert bench.sdpa_config(WORKLOADS[3], None, 1)["l2"] == "L2 flushed between steps"

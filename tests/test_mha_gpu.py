@@ -97,3 +97,32 @@ def test_mha_rejects_sizes_above_handle_maxima():
             mha.mha_forward(handle, x, x, W, W, W, W, h=4)
     finally:
         handle.close()
+
+
+@pytest.mark.parametrize("dtype,B,L,D,h", [(torch.bfloat16, 2, 300, 512, 8),
+                                           (torch.float32, 1, 128, 512, 8)])
+def test_mha_permutation_equivariance(dtype, B, L, D, h):
+    """Self-attention with no mask and no positional encoding is
+    permutation-equivariant ("The Transformer" (rayaq.ca), "Embeddings and
+    positions": reorder the words and every output is reordered with them).
+    Permuting the positions of x on the device permutes the rows of the
+    layer's output the same way, within the parity bar of the dtype; the
+    two results differ only in the order the keys are summed in."""
+    g = Draws(350 + L)
+    st = "bf16" if dtype == torch.bfloat16 else "f32"
+    x = g.normal((B, L, D), dtype=st)
+    Ws = [to_dev(g.normal((D, D), std=1.0 / np.sqrt(D), dtype=st), dtype) for _ in range(4)]
+    perm = np.stack([g.rng.permutation(L) for _ in range(B)])
+    xp = np.stack([x[b, perm[b]] for b in range(B)])
+    handle = mha.mha_create(D, dtype, B, L, L)
+    try:
+        dx, dxp = to_dev(x, dtype), to_dev(xp, dtype)
+        out = to_np(mha.mha_forward(handle, dx, dx, *Ws, h=h))
+        out_p = to_np(mha.mha_forward(handle, dxp, dxp, *Ws, h=h))
+        assert mha.mha_check(handle) == mha.MHA_OK
+    finally:
+        handle.close()
+    moved = np.stack([out[b, perm[b]] for b in range(B)])
+    assert not np.array_equal(xp, x)
+    max_abs, rms = assert_parity(out_p, moved, dtype, "permuted positions")
+    print(f"\npermutation {st}: max|out(Px) - P out(x)| {max_abs:.3e}, rms rel {rms:.3e}")

@@ -1,7 +1,8 @@
 """The four attention workloads at full size, called exactly as bench.py
 calls them, against the fp64 oracle: every output of the key-padding
-encoder workload, and seeded row samples (plus fixed tile-edge rows) of the
-causal decoder, cross-attention and long-context workloads."""
+encoder, decoder causal and cross-attention workloads, and seeded row
+samples (plus fixed tile-edge rows) of the long-context workload, whose
+8.8 TFLOP the oracle cannot finish in seconds."""
 import numpy as np
 import pytest
 import torch
@@ -30,21 +31,25 @@ def gpu_run(w, Q, K, V, lens, out_dtype=torch.bfloat16):
     return O
 
 
-def test_encoder_key_padding_full_output():
-    w = WORKLOADS[2]
+@pytest.mark.parametrize("wid", [2, 3, 4])
+def test_workload_full_output(wid):
+    """Every output element of the workload (B32 L512 key padding: 16.8 M
+    values; B16 L2048 causal: 33.6 M; B64 Lq256 Lk1024: 8.4 M)."""
+    w = WORKLOADS[wid]
     Q, K, V, lens, _ = sdpa_inputs(w)
-    assert lens.min() >= 256 and lens.max() <= 512
+    if lens is not None:
+        assert lens.min() >= 256 and lens.max() <= 512
     got = to_np(gpu_run(w, Q, K, V, lens))
     ref = oracle.sdpa(Q, K, V, mask_kind=w.mask, key_lengths=lens)
+    assert oracle.default().last_bad_rows == 0
     max_abs, rms = assert_parity(got, ref, torch.bfloat16, w.name)
     print(f"\n{w.name}: all {got.size} outputs, max|err| {max_abs:.3e}, rms rel {rms:.3e}")
 
 
-@pytest.mark.parametrize("wid,per_head", [(3, 16), (4, 16), (5, 64)])
-def test_workload_sampled_rows(wid, per_head):
-    w = WORKLOADS[wid]
+def test_long_context_sampled_rows():
+    w = WORKLOADS[5]
     Q, K, V, lens, dims = sdpa_inputs(w)
-    rows = sample_rows(w.B, w.H, w.Lq, per_head, seed=w.seed + 1000)
+    rows = sample_rows(w.B, w.H, w.Lq, 64, seed=w.seed + 1000)
     O = gpu_run(w, Q, K, V, lens)
     got = to_np(O.reshape(-1, w.d)[torch.from_numpy(rows).cuda()])
     ref = oracle.sdpa_rows(Q, K, V, rows, mask_kind=w.mask, key_lengths=lens)

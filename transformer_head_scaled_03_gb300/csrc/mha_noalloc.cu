@@ -61,6 +61,11 @@ size_t round256(size_t n) { return (n + 255u) & ~static_cast<size_t>(255u); }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Every launch step reports through this one mapping.  The entry point
+// allocates nothing, so any CUDA failure of a step -- whatever its code --
+// is reported as MHA_ERR_CUDA, the status the header lists.
+mha_status step_status(cudaError_t e) { return e == cudaSuccess ? MHA_OK : MHA_ERR_CUDA; }
+
 }  // namespace
 }  // namespace mha
 
@@ -146,13 +151,13 @@ extern "C" mha_status mha_forward_noalloc(int d_model, mha_dtype dtype, const vo
       e = gemm(g2, ctl);
     }
   }
-  if (e != cudaSuccess) return e == cudaErrorMemoryAllocation ? MHA_ERR_OOM : MHA_ERR_CUDA;
+  if (e != cudaSuccess) return step_status(e);
   // attention per head, stored as the concatenated heads
   SdpaArgs a{q, k, v, ctx, B, heads, Lq, Lk, d,
              static_cast<float>(1.0 / sqrt(static_cast<double>(d))), mask_kind, key_lengths,
              dtype, dtype, true, cs};
   e = dtype == MHA_BF16 ? launch_sdpa_bf16(a, ctl) : launch_sdpa_f32(a, ctl);
-  if (e != cudaSuccess) return MHA_ERR_CUDA;
+  if (e != cudaSuccess) return step_status(e);
   // output projection
   GemmArgs go{};
   go.prob[0] = {ctx, Wo, out, GemmStore::kRowMajor, Lq, d};
@@ -162,6 +167,5 @@ extern "C" mha_status mha_forward_noalloc(int d_model, mha_dtype dtype, const vo
   go.K = D;
   go.dtype = dtype;
   go.stream = cs;
-  e = gemm(go, ctl);
-  return e == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
+  return step_status(gemm(go, ctl));
 }
