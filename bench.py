@@ -610,26 +610,41 @@ def bench_base_layer_cold(steps, warmup, local_rank, peaks):
             "gpu_launches_per_step": 3}
 
 
-def oracle_base_layer(n_threads_list=(0, 1), min_seconds=1.0):
-    """The oracle's base-shape layer on the host: tokens/s with all threads
-    (0) and with one."""
+def oracle_base_layer(min_seconds=1.0):
+    """The oracle's base-shape layer on the host with all its threads:
+    (tokens/s, seconds per layer, threads)."""
     from transformer_head_scaled_03_gb300.inputs import WORKLOADS, mha_inputs
     import oracle
     w = WORKLOADS[1]
     x, *Ws = mha_inputs(w)
     orc = oracle.default()
-    res = {}
-    for nt in n_threads_list:
-        orc.mha(x, x, *Ws, h=w.H, nthreads=nt)
-        n, t0 = 0, time.perf_counter()
-        while True:
-            orc.mha(x, x, *Ws, h=w.H, nthreads=nt)
-            n += 1
-            dt = time.perf_counter() - t0
-            if dt >= min_seconds:
-                break
-        res[nt] = (w.B * w.Lq * n / dt, dt / n)
-    return res, orc.num_threads()
+    orc.mha(x, x, *Ws, h=w.H)
+    n, t0 = 0, time.perf_counter()
+    while True:
+        orc.mha(x, x, *Ws, h=w.H)
+        n += 1
+        dt = time.perf_counter() - t0
+        if dt >= min_seconds:
+            break
+    return w.B * w.Lq * n / dt, dt / n, orc.num_threads()
+
+
+def oracle_base_layer_one_thread(min_seconds=1.0):
+    """The same on one thread, in a child process started with
+    OMP_NUM_THREADS=1 (so this process's oracle keeps all its threads):
+    (tokens/s, seconds per layer), or None if the child fails."""
+    code = ("import json, sys, time; sys.path.insert(0, %r)\n"
+            "import bench\n"
+            "tps, sec, th = bench.oracle_base_layer(%r)\n"
+            "print(json.dumps([tps, sec, th]))\n") % (ROOT, float(min_seconds))
+    env = dict(os.environ, OMP_NUM_THREADS="1")
+    try:
+        r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True,
+                           text=True, timeout=120, cwd=ROOT)
+        tps, sec, th = json.loads(r.stdout.strip().splitlines()[-1])
+    except Exception:
+        return None
+    return (tps, sec) if th == 1 else None
 
 
 def bench_mha_layer(w_shape, dtype_name, steps, warmup, local_rank, seed_w=None):
@@ -1106,12 +1121,14 @@ def run_gpu(args):
                      for i in (2, 3, 4)]
         base = bench_base_layer_cold(50, 5, local_rank, peaks)
         if rank == 0 and not args.skip_cpu:
-            res, cores = oracle_base_layer()
+            tps, sec, cores = oracle_base_layer()
+            one = oracle_base_layer_one_thread()
             base["cpu_baseline"] = {
-                "value": round(res[0][0], 1), "unit": "tokens/s", "cores": cores,
-                "kind": "oracle", "seconds_per_layer": round(res[0][1], 4),
-                "one_thread": {"value": round(res[1][0], 1), "unit": "tokens/s", "cores": 1,
-                               "seconds_per_layer": round(res[1][1], 4)},
+                "value": round(tps, 1), "unit": "tokens/s", "cores": cores,
+                "kind": "oracle", "seconds_per_layer": round(sec, 4),
+                "one_thread": None if one is None else {
+                    "value": round(one[0], 1), "unit": "tokens/s", "cores": 1,
+                    "seconds_per_layer": round(one[1], 4)},
                 "sample": "the whole layer (every token), fp64, repeated for ~1 s"}
         workloads.insert(0, base)
 
