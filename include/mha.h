@@ -384,13 +384,19 @@ mha_status encoder_create(mha_encoder *out, int d_model, int heads, int d_ff,
                           mha_dtype dtype, int max_batch, int max_len);
 
 /* encoder_forward -- out [B, L, D] = layer(x [B, L, D]); mask_kind and
- * key_lengths as for mha_forward (self-attention, Lq = Lk = L).  Seven
- * launches on `stream`.  out must not alias x.  Returns MHA_OK,
- * MHA_ERR_INVALID_ARG or MHA_ERR_CUDA. */
+ * key_lengths as for mha_forward (self-attention, Lq = Lk = L).
+ * out_dtype is the element type of `out`: the layer's type, or MHA_F32 for
+ * a BF16 layer (the final LayerNorm's output stored unrounded).  BF16
+ * layers with D <= 512 take five launches on `stream` (the residual add and
+ * LayerNorm run in the epilogues of the W^O and W2 GEMMs, so the sublayer
+ * outputs stay fp32 and are never stored); other layers take seven.  The
+ * hidden activation and x1 are stored in the layer's type.  out must not
+ * alias x.  Returns MHA_OK, MHA_ERR_INVALID_ARG or MHA_ERR_CUDA. */
 mha_status encoder_forward(mha_encoder enc, const void *x,
                            const mha_encoder_params *params, int B, int L,
                            int mask_kind, const int32_t *key_lengths,
-                           float ln_eps, void *out, mha_stream stream);
+                           float ln_eps, void *out, mha_dtype out_dtype,
+                           mha_stream stream);
 
 /* encoder_destroy -- free the handle (synchronises the device).  NULL is
  * accepted. */

@@ -1,10 +1,12 @@
 """encoder_forward (MHA with biases, residual + LayerNorm, ReLU FFN,
 residual + LayerNorm) on the GPU against the fp64 oracle.
 
-Tolerances: fp32 max|err| <= 1e-4.  bf16: max|err| <= 5e-2 and RMS relative
-<= 1e-2 -- the layer output is a LayerNorm output with |y| up to ~5, where a
-bf16 half-ulp alone is 0.0156, and four intermediate tensors (Q/K/V, context,
-x1, the FFN hidden activation) are rounded to bf16 on the way."""
+Tolerances: an fp32 layer, max|err| <= 1e-4.  A bf16 layer is graded on its
+output kept in fp32 (out_dtype float32): max|err| <= 2e-2 and RMS relative
+<= 1e-2, the bar for bf16 inputs with fp32 accumulation.  Its bf16 output is
+that same result rounded once more; the test reports its error and bounds it
+by the bar plus the rounding's own half-ulp, 2^-8 of the largest |y|
+(LayerNorm outputs reach |y| ~ 5, where half an ulp is 0.0156)."""
 import numpy as np
 import pytest
 import torch
@@ -17,7 +19,7 @@ from tests.gpu_util import errors, to_dev, to_np
 
 pytestmark = pytest.mark.gpu
 
-BF16_MAX, BF16_RMS, F32_MAX = 5e-2, 1e-2, 1e-4
+from tests.gpu_util import BF16_MAX_ABS as BF16_MAX, BF16_RMS_REL as BF16_RMS, F32_MAX_ABS as F32_MAX
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -46,6 +48,10 @@ CASES = [
     (torch.bfloat16, 2, 128, 512, 8, 2048, mha.MASK_NONE, None),
     (torch.bfloat16, 1, 200, 256, 4, 1024, mha.MASK_CAUSAL, None),
     (torch.bfloat16, 3, 64, 512, 4, 512, mha.MASK_KEY_PADDING, [64, 10, 33]),
+    # d_model 384: the fused epilogue's MMA split 256 + 128 columns, 100 rows
+    (torch.bfloat16, 1, 100, 384, 6, 1536, mha.MASK_NONE, None),
+    # d_model 1024: the seven-launch form (residual + LayerNorm as own launches)
+    (torch.bfloat16, 2, 96, 1024, 8, 1024, mha.MASK_CAUSAL, None),
     (torch.float32, 1, 128, 512, 8, 2048, mha.MASK_NONE, None),
     (torch.float32, 2, 50, 96, 3, 200, mha.MASK_CAUSAL, None),
 ]
@@ -61,20 +67,33 @@ def test_encoder_layer_parity(case):
     lens = np.asarray(lengths, np.int32) if lengths else None
     layer = mha.EncoderLayer(D, h, F, dtype, B, L)
     try:
-        out = layer.forward(to_dev(x, dtype), {k: to_dev(v, dtype) for k, v in p.items()},
-                            mask_kind=mk,
-                            key_lengths=torch.from_numpy(lens).cuda() if lens is not None else None)
+        dx = to_dev(x, dtype)
+        dp = {k: to_dev(v, dtype) for k, v in p.items()}
+        kl = torch.from_numpy(lens).cuda() if lens is not None else None
+        out = layer.forward(dx, dp, mask_kind=mk, key_lengths=kl)
+        out32 = (layer.forward(dx, dp, mask_kind=mk, key_lengths=kl, out_dtype=torch.float32)
+                 if dtype == torch.bfloat16 else None)
         assert mha.mha_check() == mha.MHA_OK
         got = to_np(out)
+        got32 = to_np(out32) if out32 is not None else None
+        rounded = out32.to(torch.bfloat16) if out32 is not None else None
     finally:
         layer.close()
     ref = oracle.encoder_layer(x, p, h, mask_kind=mk, key_lengths=lens)
     max_abs, rms = errors(got, ref)
     if dtype == torch.bfloat16:
-        assert max_abs <= BF16_MAX and rms <= BF16_RMS, (case, max_abs, rms)
+        max32, rms32 = errors(got32, ref)
+        assert max32 <= BF16_MAX and rms32 <= BF16_RMS, (case, "fp32 out", max32, rms32)
+        bound = BF16_MAX + 2.0 ** -8 * float(np.max(np.abs(ref)))
+        assert max_abs <= bound and rms <= BF16_RMS, (case, "bf16 out", max_abs, bound, rms)
+        if D <= 512:
+            # one kernel computes both; only the final store differs
+            assert torch.equal(rounded, out), case
+        print(f"\nencoder {case[1:6]} bf16: fp32 out max|err| {max32:.3e} rms rel {rms32:.3e}; "
+              f"bf16 out max|err| {max_abs:.3e} (bound {bound:.3e}) rms rel {rms:.3e}")
     else:
         assert max_abs <= F32_MAX, (case, max_abs)
-    print(f"\nencoder {case[1:6]} {st}: max|err| {max_abs:.3e} rms rel {rms:.3e}")
+        print(f"\nencoder {case[1:6]} {st}: max|err| {max_abs:.3e} rms rel {rms:.3e}")
 
 
 def test_encoder_rejects_unsupported_shapes():

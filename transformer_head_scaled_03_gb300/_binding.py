@@ -86,7 +86,7 @@ def _declare(lib):
     lib.encoder_create.argtypes = [ctypes.POINTER(vp), i32, i32, i32, i32, i32, i32]
     lib.encoder_create.restype = i32
     lib.encoder_forward.argtypes = [vp, vp, ctypes.POINTER(EncoderParams), i32, i32, i32, vp,
-                                    f32, vp, vp]
+                                    f32, vp, i32, vp]
     lib.encoder_forward.restype = i32
     lib.encoder_destroy.argtypes = [vp]
     lib.encoder_destroy.restype = i32
@@ -382,7 +382,9 @@ class EncoderLayer:
         self.d_model, self.heads, self.d_ff, self.dtype = d_model, heads, d_ff, dtype
 
     def forward(self, x, params: dict, mask_kind: int = MASK_NONE, key_lengths=None,
-                ln_eps: float = 1e-5, out=None, stream=None):
+                ln_eps: float = 1e-5, out=None, stream=None, out_dtype=None):
+        """``out_dtype``: the layer's dtype (default), or torch.float32 for a
+        bf16 layer to keep the final LayerNorm's output unrounded."""
         if self._h is None:
             raise RuntimeError("encoder destroyed")
         B, L, D = x.shape
@@ -395,11 +397,14 @@ class EncoderLayer:
             if tuple(t.shape) != want or t.dtype != self.dtype:
                 raise ValueError(f"parameter {n} must be {want} {self.dtype}")
         p = EncoderParams(*[_dev_ptr(params[n]) for n in ENCODER_PARAM_NAMES])
+        odt = self.dtype if out_dtype is None else out_dtype
         if out is None:
-            out = torch.empty_like(x)
+            out = torch.empty(x.shape, dtype=odt, device=x.device)
+        if out.dtype != odt or tuple(out.shape) != tuple(x.shape):
+            raise ValueError("out does not match the output dtype and shape")
         st = lib().encoder_forward(self._h, _dev_ptr(x), ctypes.byref(p), B, L, int(mask_kind),
                                    _dev_ptr(key_lengths), float(ln_eps), _dev_ptr(out),
-                                   _stream(stream))
+                                   _dtype_code(odt), _stream(stream))
         _check(st, "encoder_forward")
         return out
 

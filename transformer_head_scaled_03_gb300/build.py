@@ -18,7 +18,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libmha_gb300.so")
-SOURCES = ["mha_api.cu", "sdpa_bf16.cu", "gemm_bf16.cu", "fp32_path.cu", "mha_noalloc.cu",
+SOURCES = ["mha_api.cu", "sdpa_bf16.cu", "gemm_bf16.cu", "gemm_ln_bf16.cu", "fp32_path.cu",
+           "mha_noalloc.cu",
            "layernorm.cu", "encoder_api.cu", "sdpa_decode.cu",
            "embed_pe.cu", "sdpa_backward.cu", "host_pipeline.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

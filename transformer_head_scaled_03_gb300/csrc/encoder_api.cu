@@ -4,12 +4,16 @@
 //   a   = MultiHead(x, x, x) with biases      (GEMM with bias epilogue and
 //                                               head-split store, attention
 //                                               with concat store, GEMM + bo)
-//   x1  = LayerNorm1(x + a)                   (add_layernorm)
+//   x1  = LayerNorm1(x + a)
 //   f   = max(0, x1 W1 + b1) W2 + b2          (GEMM bias+ReLU, GEMM bias)
-//   out = LayerNorm2(x1 + f)                  (add_layernorm)
+//   out = LayerNorm2(x1 + f)
 // ("The Transformer" (hoshank.vercel.app), "The Mathematics"; "The
 // Transformer" (rayaq.ca), "The feed-forward block", "Residuals and
-// LayerNorm", "The encoder stack".)  Seven launches on one stream.
+// LayerNorm", "The encoder stack".)
+// bf16 layers with d_model <= 512 run five launches: the residual add and
+// LayerNorm are the epilogues of the W^O and W2 GEMMs (gemm_ln_bf16), so a
+// and f stay in fp32 and never reach memory.  Other layers run seven: each
+// GEMM stores its output and add_layernorm reads it back.
 #include <math.h>
 #include <stdint.h>
 
@@ -100,8 +104,10 @@ mha_status encoder_create(mha_encoder* out, int d_model, int heads, int d_ff, mh
 
 mha_status encoder_forward(mha_encoder c, const void* x, const mha_encoder_params* w, int B,
                            int L, int mask_kind, const int32_t* key_lengths, float ln_eps,
-                           void* out, mha_stream stream) {
+                           void* out, mha_dtype out_dtype, mha_stream stream) {
   if (!c || !w) return MHA_ERR_INVALID_ARG;
+  if (out_dtype != c->dtype && !(c->dtype == MHA_BF16 && out_dtype == MHA_F32))
+    return MHA_ERR_INVALID_ARG;
   if (B < 0 || L < 1 || B > c->max_batch || L > c->max_len) return MHA_ERR_INVALID_ARG;
   if (!(ln_eps >= 0.f) || isinf(ln_eps)) return MHA_ERR_INVALID_ARG;
   if (mask_kind < 0 || mask_kind > (MHA_MASK_CAUSAL | MHA_MASK_KEY_PADDING))
@@ -154,14 +160,28 @@ mha_status encoder_forward(mha_encoder c, const void* x, const mha_encoder_param
              c->dtype, c->dtype, true, s, nullptr, 0, 0};
   e = c->dtype == MHA_BF16 ? launch_sdpa_bf16(a, ctl) : launch_sdpa_f32(a, ctl);
   if (e != cudaSuccess) return status_of(e);
+  if (c->dtype == MHA_BF16 && gemm_ln_bf16_supported(D)) {
+    // x1 = LN1(x + ctx Wo + bo); hid = relu(x1 W1 + b1); out = LN2(x1 + hid W2 + b2)
+    auto gemm_ln = [&](const void* A, const void* W, const void* bias, const void* resid,
+                       const void* gamma, const void* beta, void* C, mha_dtype odt, int K) {
+      GemmLnArgs g{A, W, bias, resid, gamma, beta, ln_eps, C, odt, M, D, K, s};
+      return launch_gemm_ln_bf16(g, ctl);
+    };
+    if ((e = gemm_ln(c->ctx, w->Wo, w->bo, x, w->ln1_gamma, w->ln1_beta, c->x1, MHA_BF16, D)) !=
+        cudaSuccess)
+      return status_of(e);
+    if ((e = gemm1(c->x1, w->W1, c->hid, w->b1, 1, F, D)) != cudaSuccess) return status_of(e);
+    return status_of(gemm_ln(c->hid, w->W2, w->b2, c->x1, w->ln2_gamma, w->ln2_beta, out,
+                             out_dtype, F));
+  }
   if ((e = gemm1(c->ctx, w->Wo, c->tmp, w->bo, 0, D, D)) != cudaSuccess) return status_of(e);
   if ((e = launch_add_layernorm(x, c->tmp, w->ln1_gamma, w->ln1_beta, ln_eps, c->x1, M, D,
-                                c->dtype, s)) != cudaSuccess)
+                                c->dtype, c->dtype, s)) != cudaSuccess)
     return status_of(e);
   if ((e = gemm1(c->x1, w->W1, c->hid, w->b1, 1, F, D)) != cudaSuccess) return status_of(e);
   if ((e = gemm1(c->hid, w->W2, c->tmp, w->b2, 0, D, F)) != cudaSuccess) return status_of(e);
   return status_of(launch_add_layernorm(c->x1, c->tmp, w->ln2_gamma, w->ln2_beta, ln_eps, out, M,
-                                        D, c->dtype, s));
+                                        D, c->dtype, out_dtype, s));
 }
 
 mha_status encoder_destroy(mha_encoder c) {

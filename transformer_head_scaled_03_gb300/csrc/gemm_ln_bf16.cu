@@ -1,0 +1,407 @@
+// gemm_ln_bf16.cu -- a projection whose epilogue is the post-norm sublayer
+// wrapper: C = LayerNorm(R + A @ W + bias) * gamma + beta, bf16 operands,
+// fp32 accumulation and statistics, on sm_103a tcgen05 tensor cores.
+//
+// In the post-norm encoder layer every sublayer's output is added to its
+// input and the sum is normalised per position ("The Transformer"
+// (hoshank.vercel.app), "The Mathematics": output = LayerNorm(x +
+// Sublayer(x)); "The Transformer" (rayaq.ca), "Residuals and LayerNorm").
+// The attention output projection (R = x) and the second FFN matrix
+// (R = x1) are the last steps of their sublayers, so the residual add and
+// the LayerNorm run in those GEMMs' epilogues: the sublayer output never
+// goes to memory, and it is never rounded to bf16 before the sum.
+//
+// A CTA's output tile is 128 rows x N columns with N = d_model <= 512, i.e.
+// whole rows: the fp32 accumulator holds N of the 512 tensor-memory columns
+// and each epilogue thread owns one row.  The epilogue makes two passes
+// over the row in tensor memory:
+//   1. v = acc + bias + R (R read through a shared-memory transpose so that
+//      each load instruction moves four whole 128-byte row pieces); per
+//      64-column chunk the mean and the centred sum of squares, merged
+//      chunk by chunk with the pairwise update of Chan, Golub and LeVeque
+//      ("Updating formulae and a pairwise algorithm for computing sample
+//      variances", 1979): no E[v^2] - E[v]^2 cancellation; v goes back into
+//      tensor memory;
+//   2. y = (v - mean) / sqrt(var + eps) * gamma + beta, population variance
+//      (divisor N), stored as bf16 or fp32 through the same transpose.
+// Warp roles and the TMA ring are those of the plain projection kernel:
+// warp 0 TMA producer, warp 1 MMA issuer and TMEM owner, warps 2-5 epilogue.
+// One accumulator: the next tile's MMAs wait for the epilogue, while the TMA
+// ring keeps loading ahead.
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace mha {
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kBK = 64;
+constexpr int kABytes = kBM * kBK * 2;  // 16 KB: 128 rows x 64 k
+constexpr int kWBox = 64 * 64 * 2;      // 8 KB: one 64(N) x 64(K) box of W
+constexpr int kThreads = 192;
+constexpr int kStageWarpBytes = 32 * 128;  // epilogue staging: 32 rows x 128 bytes
+
+template <int NB>  // N = 64 * NB output columns = whole rows
+struct LnCfg {
+  static_assert(NB >= 1 && NB <= 8, "N = 64..512");
+  static constexpr int N = 64 * NB;
+  static constexpr int kStageBytes = kABytes + NB * kWBox;
+  static constexpr int kStages = 4 * kStageBytes <= 196608 ? 4 : 3 * kStageBytes <= 196608 ? 3 : 2;
+  static constexpr uint32_t kTmemCols = N <= 64 ? 64u : N <= 128 ? 128u : N <= 256 ? 256u : 512u;
+  // MMA column chunks of at most 256 (the largest N of one M = 128 MMA)
+  static constexpr int kChunks = (N + 255) / 256;
+  __host__ __device__ static constexpr int chunk_n(int c) { return N - 256 * c < 256 ? N - 256 * c : 256; }
+  // barriers: full[S], empty[S], acc_full, acc_empty, drain
+  __host__ __device__ static constexpr int bFull(int s) { return s; }
+  __host__ __device__ static constexpr int bEmpty(int s) { return kStages + s; }
+  static constexpr int bAccFull = 2 * kStages;
+  static constexpr int bAccEmpty = 2 * kStages + 1;
+  static constexpr int bDrain = 2 * kStages + 2;
+  static constexpr int kNumBars = 2 * kStages + 3;
+  static constexpr int kOffBar = kStages * kStageBytes;
+  static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
+  static constexpr int kOffStage = (kOffMisc + 16 + 127) & ~127;
+  static constexpr int kSmemBytes = kOffStage + 4 * kStageWarpBytes + 1024;
+  static_assert(kSmemBytes <= 232448, "shared memory");
+};
+
+struct GemmLnParams {
+  void* C;                          // [M, N], bf16 or fp32
+  const __nv_bfloat16* bias;        // [N]
+  const __nv_bfloat16* resid;       // [M, N]
+  const __nv_bfloat16* gamma;       // [N]
+  const __nv_bfloat16* beta;        // [N]
+  float eps;
+  int out_f32;
+  int M, K;
+  int mt;                           // row tiles
+  unsigned* err;
+  uint64_t limit_ns;
+};
+
+__device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_timer_ns() - t0 > limit_ns) return;
+  }
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+template <int NB>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_ln_bf16_kernel(const __grid_constant__ CUtensorMap tA,
+                        const __grid_constant__ CUtensorMap tW, const GemmLnParams p) {
+  using C = LnCfg<NB>;
+  constexpr int N = C::N;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + C::kOffMisc);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kOffMisc + 4);
+  auto bar = [base](int i) -> uint32_t { return base + C::kOffBar + 8u * i; };
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const WaitCtl ctl{abort_flag, p.err, p.limit_ns};
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(bar(C::bFull(s)), 1);
+      mbar_init(bar(C::bEmpty(s)), 1);
+    }
+    mbar_init(bar(C::bAccFull), 1);
+    mbar_init(bar(C::bAccEmpty), 128);
+    mbar_init(bar(C::bDrain), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc<C::kTmemCols>(smem_u32(tmem_slot));
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tA);
+    tma_prefetch_desc(&tW);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+  const int num_k = (p.K + kBK - 1) / kBK;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int g = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < p.mt; t += gridDim.x) {
+        const int m0 = t * kBM;
+        for (int kt = 0; kt < num_k; ++kt, ++g) {
+          const int st = g % C::kStages;
+          const uint32_t ph = (g / C::kStages) & 1;
+          if (!(ok = mbar_wait(bar(C::bEmpty(st)), ph ^ 1u, ctl))) break;
+          const uint32_t sa = base + st * C::kStageBytes;
+          mbar_expect_tx(bar(C::bFull(st)), C::kStageBytes);
+          tma_load_2d(sa, &tA, bar(C::bFull(st)), kt * kBK, m0);
+#pragma unroll
+          for (int nb = 0; nb < NB; ++nb)
+            tma_load_2d(sa + kABytes + nb * kWBox, &tW, bar(C::bFull(st)), nb * 64, kt * kBK);
+        }
+      }
+      for (int q = max(0, g - C::kStages); q < g; ++q)
+        wait_drain(bar(C::bFull(q % C::kStages)), (q / C::kStages) & 1, p.limit_ns);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      int g = 0, i = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < p.mt; t += gridDim.x, ++i) {
+        // the single accumulator, once the epilogue has drained the last tile
+        if (!(ok = mbar_wait(bar(C::bAccEmpty), (i & 1) ^ 1u, ctl))) break;
+        tc_fence_after();
+        for (int kt = 0; kt < num_k; ++kt, ++g) {
+          const int st = g % C::kStages;
+          const uint32_t ph = (g / C::kStages) & 1;
+          if (!(ok = mbar_wait(bar(C::bFull(st)), ph, ctl))) break;
+          tc_fence_after();
+          const uint32_t sa = base + st * C::kStageBytes;
+          const uint32_t sw = sa + kABytes;
+#pragma unroll
+          for (int ks = 0; ks < kBK / 16; ++ks) {
+#pragma unroll
+            for (int c = 0; c < C::kChunks; ++c) {
+              // A: K-major, +32 bytes per 16 k; W: MN-major, +16 rows of 128
+              // bytes per 16 k, 64-column boxes kWBox apart
+              umma_ss(tmem + static_cast<uint32_t>(256 * c), sdesc_sw128(sa + ks * 32, 16, 1024),
+                      sdesc_sw128(sw + c * 4 * kWBox + ks * 16 * 128, kWBox, 1024),
+                      idesc_bf16_f32(kBM, C::chunk_n(c), false, true),
+                      (kt > 0 || ks > 0) ? 1u : 0u);
+            }
+          }
+          umma_commit(bar(C::bEmpty(st)));
+        }
+        if (ok) umma_commit(bar(C::bAccFull));
+      }
+      umma_commit(bar(C::bDrain));
+      wait_drain(bar(C::bDrain), 0, p.limit_ns);
+    }
+  } else {
+    // epilogue: warp w may touch TMEM lanes [32 (w % 4), 32 (w % 4) + 32)
+    const int quarter = warp & 3;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    uint4* stg = reinterpret_cast<uint4*>(gbase + C::kOffStage + (warp - 2) * kStageWarpBytes);
+    const int q = lane & 7;  // the 16-byte piece this lane moves in the transposes
+    int i = 0;
+    for (int t = blockIdx.x; t < p.mt; t += gridDim.x, ++i) {
+      const bool ok = num_k > 0 && mbar_wait_warp(bar(C::bAccFull), i & 1, ctl);
+      if (!ok) break;
+      tc_fence_after();
+      const int row0 = t * kBM + quarter * 32;  // this warp's first row
+      // ---- pass 1: v = acc + bias + R, row statistics, v back to TMEM
+      float mean = 0.f, m2 = 0.f;
+#pragma unroll 1
+      for (int cb = 0; cb < NB; ++cb) {
+        const int n = cb * 64;
+        uint32_t v[64];
+        tmem_ld32(lane_base + n, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+        tmem_ld32(lane_base + n + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+        // the warp's 32 residual rows, 64 columns: lane l loads piece l % 8
+        // of row 4 g4 + l / 8 (four whole 128-byte row pieces per
+        // instruction); piece qq of row r sits at slot qq ^ (r & 7)
+#pragma unroll
+        for (int g4 = 0; g4 < 8; ++g4) {
+          const int rr = 4 * g4 + (lane >> 3);
+          uint4 w = make_uint4(0u, 0u, 0u, 0u);
+          if (row0 + rr < p.M)
+            w = __ldg(reinterpret_cast<const uint4*>(p.resid + static_cast<size_t>(row0 + rr) * N +
+                                                     n) + q);
+          stg[rr * 8 + (q ^ (rr & 7))] = w;
+        }
+        __syncwarp();
+        tmem_ld_wait(v);
+        float s = 0.f;
+#pragma unroll
+        for (int qq = 0; qq < 8; ++qq) {
+          const uint4 r = stg[lane * 8 + (qq ^ (lane & 7))];
+          const uint4 b = __ldg(reinterpret_cast<const uint4*>(p.bias + n) + qq);
+          const uint32_t rw[4] = {r.x, r.y, r.z, r.w};
+          const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float lo = __uint_as_float(v[8 * qq + 2 * k]) + bf16_lo(bw[k]) + bf16_lo(rw[k]);
+            const float hi =
+                __uint_as_float(v[8 * qq + 2 * k + 1]) + bf16_hi(bw[k]) + bf16_hi(rw[k]);
+            v[8 * qq + 2 * k] = __float_as_uint(lo);
+            v[8 * qq + 2 * k + 1] = __float_as_uint(hi);
+            s += lo + hi;
+          }
+        }
+        __syncwarp();  // the staging rows are rewritten by the next chunk
+        // this chunk's mean and centred sum of squares, then the pairwise merge
+        const float mc = s * (1.f / 64.f);
+        float qc = 0.f;
+#pragma unroll
+        for (int k = 0; k < 64; ++k) {
+          const float d = __uint_as_float(v[k]) - mc;
+          qc = fmaf(d, d, qc);
+        }
+        if (cb == 0) {
+          mean = mc;
+          m2 = qc;
+        } else {
+          const float na = 64.f * cb, nt = na + 64.f;
+          const float delta = mc - mean;
+          mean = fmaf(delta, 64.f / nt, mean);
+          m2 = m2 + qc + delta * delta * (na * 64.f / nt);
+        }
+        tmem_st32(lane_base + n, *reinterpret_cast<const uint32_t(*)[32]>(&v[0]));
+        tmem_st32(lane_base + n + 32, *reinterpret_cast<const uint32_t(*)[32]>(&v[32]));
+      }
+      tmem_st_wait();
+      const float inv = 1.f / sqrtf(m2 * (1.f / static_cast<float>(N)) + p.eps);
+      // ---- pass 2: y = (v - mean) * inv * gamma + beta, stored row-major
+#pragma unroll 1
+      for (int cb = 0; cb < NB; ++cb) {
+        const int n = cb * 64;
+        uint32_t v[64];
+        tmem_ld32(lane_base + n, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+        tmem_ld32(lane_base + n + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+        tmem_ld_wait(v);
+#pragma unroll
+        for (int qq = 0; qq < 8; ++qq) {
+          const uint4 gv = __ldg(reinterpret_cast<const uint4*>(p.gamma + n) + qq);
+          const uint4 bv = __ldg(reinterpret_cast<const uint4*>(p.beta + n) + qq);
+          const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+          const uint32_t bw[4] = {bv.x, bv.y, bv.z, bv.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float lo = fmaf((__uint_as_float(v[8 * qq + 2 * k]) - mean) * inv, bf16_lo(gw[k]),
+                                  bf16_lo(bw[k]));
+            const float hi = fmaf((__uint_as_float(v[8 * qq + 2 * k + 1]) - mean) * inv,
+                                  bf16_hi(gw[k]), bf16_hi(bw[k]));
+            v[8 * qq + 2 * k] = __float_as_uint(lo);
+            v[8 * qq + 2 * k + 1] = __float_as_uint(hi);
+          }
+        }
+        if (!p.out_f32) {
+#pragma unroll
+          for (int qq = 0; qq < 8; ++qq) {
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(v[8 * qq + 0]), __uint_as_float(v[8 * qq + 1]));
+            w.y = pack_bf16x2(__uint_as_float(v[8 * qq + 2]), __uint_as_float(v[8 * qq + 3]));
+            w.z = pack_bf16x2(__uint_as_float(v[8 * qq + 4]), __uint_as_float(v[8 * qq + 5]));
+            w.w = pack_bf16x2(__uint_as_float(v[8 * qq + 6]), __uint_as_float(v[8 * qq + 7]));
+            stg[lane * 8 + (qq ^ (lane & 7))] = w;
+          }
+          __syncwarp();
+          __nv_bfloat16* Cb = static_cast<__nv_bfloat16*>(p.C);
+#pragma unroll
+          for (int g4 = 0; g4 < 8; ++g4) {
+            const int rr = 4 * g4 + (lane >> 3);
+            const uint4 w = stg[rr * 8 + (q ^ (rr & 7))];
+            if (row0 + rr < p.M)
+              reinterpret_cast<uint4*>(Cb + static_cast<size_t>(row0 + rr) * N + n)[q] = w;
+          }
+          __syncwarp();
+        } else {
+          // fp32: 32 columns (128 bytes) of every row per round
+          float* Cf = static_cast<float*>(p.C);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+#pragma unroll
+            for (int qq = 0; qq < 8; ++qq)
+              stg[lane * 8 + (qq ^ (lane & 7))] =
+                  make_uint4(v[32 * h + 4 * qq], v[32 * h + 4 * qq + 1], v[32 * h + 4 * qq + 2],
+                             v[32 * h + 4 * qq + 3]);
+            __syncwarp();
+#pragma unroll
+            for (int g4 = 0; g4 < 8; ++g4) {
+              const int rr = 4 * g4 + (lane >> 3);
+              const uint4 w = stg[rr * 8 + (q ^ (rr & 7))];
+              if (row0 + rr < p.M)
+                reinterpret_cast<uint4*>(Cf + static_cast<size_t>(row0 + rr) * N + n + 32 * h)[q] = w;
+            }
+            __syncwarp();
+          }
+        }
+      }
+      // the accumulator may take the next tile
+      tc_fence_before();
+      mbar_arrive(bar(C::bAccEmpty));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc<C::kTmemCols>(tmem);
+}
+
+int current_sm_count() {
+  int dev = 0, v = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess &&
+      cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0)
+    return v;
+  return 1;
+}
+
+template <int NB>
+cudaError_t launch_nb(const GemmLnArgs& g, const DeviceCtl& ctl) {
+  using C = LnCfg<NB>;
+  CUtensorMap ta, tw;
+  const uint64_t adims[2] = {static_cast<uint64_t>(g.K), static_cast<uint64_t>(g.M)};
+  const uint64_t astr[1] = {static_cast<uint64_t>(g.K) * 2};
+  const uint32_t abox[2] = {64, 128};
+  const uint64_t wdims[2] = {static_cast<uint64_t>(C::N), static_cast<uint64_t>(g.K)};
+  const uint64_t wstr[1] = {static_cast<uint64_t>(C::N) * 2};
+  const uint32_t wbox[2] = {64, 64};
+  if (!encode_tensor_map(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(g.A), adims,
+                         astr, abox, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_tensor_map(&tw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(g.W), wdims,
+                         wstr, wbox, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  GemmLnParams p{};
+  p.C = g.C;
+  p.bias = static_cast<const __nv_bfloat16*>(g.bias);
+  p.resid = static_cast<const __nv_bfloat16*>(g.resid);
+  p.gamma = static_cast<const __nv_bfloat16*>(g.gamma);
+  p.beta = static_cast<const __nv_bfloat16*>(g.beta);
+  p.eps = g.eps;
+  p.out_f32 = g.out_dtype == MHA_F32 ? 1 : 0;
+  p.M = g.M;
+  p.K = g.K;
+  p.mt = (g.M + kBM - 1) / kBM;
+  p.err = ctl.err;
+  p.limit_ns = ctl.limit_ns;
+  auto kern = gemm_ln_bf16_kernel<NB>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  // one CTA per SM at most (tensor memory and shared memory admit no second)
+  const int sms = current_sm_count();
+  const int grid = p.mt < sms ? p.mt : sms;
+  kern<<<grid, kThreads, C::kSmemBytes, g.stream>>>(ta, tw, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool gemm_ln_bf16_supported(int N) { return N >= 64 && N <= 512 && N % 64 == 0; }
+
+cudaError_t launch_gemm_ln_bf16(const GemmLnArgs& g, const DeviceCtl& ctl) {
+  if (g.M == 0) return cudaSuccess;
+  if (!gemm_ln_bf16_supported(g.N) || g.K < 1) return cudaErrorInvalidValue;
+  switch (g.N / 64) {
+    case 1: return launch_nb<1>(g, ctl);
+    case 2: return launch_nb<2>(g, ctl);
+    case 3: return launch_nb<3>(g, ctl);
+    case 4: return launch_nb<4>(g, ctl);
+    case 5: return launch_nb<5>(g, ctl);
+    case 6: return launch_nb<6>(g, ctl);
+    case 7: return launch_nb<7>(g, ctl);
+    default: return launch_nb<8>(g, ctl);
+  }
+}
+
+}  // namespace mha

@@ -62,10 +62,34 @@ struct DeviceCtl {
 };
 
 // out[m, :] = LayerNorm(a[m, :] + b[m, :]) * gamma + beta over rows of width D
-// (population variance, eps), fp32 statistics; element type `dt` for all.
+// (population variance, eps), fp32 statistics; element type `dt` for a, b,
+// gamma and beta, `out_dt` for out (F32 out of a BF16 layer keeps the last
+// LayerNorm's output unrounded).
 cudaError_t launch_add_layernorm(const void* a, const void* b, const void* gamma,
                                  const void* beta, float eps, void* out, long M, int D,
-                                 mha_dtype dt, cudaStream_t stream);
+                                 mha_dtype dt, mha_dtype out_dt, cudaStream_t stream);
+
+// C[M, N] = LayerNorm(resid + A[M, K] @ W[K, N] + bias) * gamma + beta, the
+// residual add and LayerNorm in the GEMM epilogue (bf16 operands, fp32
+// accumulator and statistics, population variance); N = 64..512 in steps of
+// 64 so that one CTA holds whole rows.  C is bf16, or fp32 when out_dtype is
+// MHA_F32.
+struct GemmLnArgs {
+  const void* A;      // [M, K] bf16
+  const void* W;      // [K, N] bf16
+  const void* bias;   // [N] bf16
+  const void* resid;  // [M, N] bf16
+  const void* gamma;  // [N] bf16
+  const void* beta;   // [N] bf16
+  float eps;
+  void* C;
+  mha_dtype out_dtype;
+  int M, N, K;
+  cudaStream_t stream;
+};
+
+bool gemm_ln_bf16_supported(int N);
+cudaError_t launch_gemm_ln_bf16(const GemmLnArgs& g, const DeviceCtl& ctl);
 
 // Device error bits of the embedding pass and the backward pass (ptx.cuh
 // holds the others).

@@ -34,12 +34,12 @@ __device__ __forceinline__ float lane_sum(float v) {
 
 constexpr int kRowsPerBlock = 4;
 
-// VPL: values per lane held in registers (D <= 32 * VPL)
-template <typename T, int VPL>
+// VPL: values per lane held in registers (D <= 32 * VPL); TO: output type
+template <typename T, int VPL, typename TO = T>
 __global__ void __launch_bounds__(32 * kRowsPerBlock)
     add_layernorm_kernel(const T* __restrict__ a, const T* __restrict__ b,
                          const T* __restrict__ gamma, const T* __restrict__ beta, float eps,
-                         T* __restrict__ out, long M, int D) {
+                         TO* __restrict__ out, long M, int D) {
   const int lane = threadIdx.x & 31;
   const long row = static_cast<long>(blockIdx.x) * kRowsPerBlock + (threadIdx.x >> 5);
   if (row >= M) return;  // whole warp leaves together
@@ -63,11 +63,11 @@ __global__ void __launch_bounds__(32 * kRowsPerBlock)
   }
   const float var = lane_sum(sq) / static_cast<float>(D);
   const float inv = 1.f / sqrtf(var + eps);
-  T* orow = out + row * D;
+  TO* orow = out + row * D;
 #pragma unroll
   for (int i = 0; i < VPL; ++i) {
     const int c = lane + 32 * i;
-    if (c < D) orow[c] = from_f<T>((v[i] - mean) * inv * to_f(gamma[c]) + to_f(beta[c]));
+    if (c < D) orow[c] = from_f<TO>((v[i] - mean) * inv * to_f(gamma[c]) + to_f(beta[c]));
   }
 }
 
@@ -158,12 +158,33 @@ cudaError_t launch_typed(const void* a, const void* b, const void* g, const void
   return cudaGetLastError();
 }
 
+// bf16 inputs, fp32 output (row by row; the layer's last LayerNorm only)
+cudaError_t launch_bf16_to_f32(const void* a, const void* b, const void* g, const void* be,
+                               float eps, void* out, long M, int D, cudaStream_t s) {
+  using T = __nv_bfloat16;
+  const dim3 grid(static_cast<unsigned>((M + kRowsPerBlock - 1) / kRowsPerBlock));
+  const dim3 block(32 * kRowsPerBlock);
+  auto args = [&](auto kern) {
+    kern<<<grid, block, 0, s>>>(static_cast<const T*>(a), static_cast<const T*>(b),
+                                static_cast<const T*>(g), static_cast<const T*>(be), eps,
+                                static_cast<float*>(out), M, D);
+  };
+  if (D <= 32 * 16) args(add_layernorm_kernel<T, 16, float>);
+  else if (D <= 32 * 32) args(add_layernorm_kernel<T, 32, float>);
+  else if (D <= 32 * 128) args(add_layernorm_kernel<T, 128, float>);
+  else return cudaErrorInvalidValue;
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_add_layernorm(const void* a, const void* b, const void* gamma,
                                  const void* beta, float eps, void* out, long M, int D,
-                                 mha_dtype dt, cudaStream_t stream) {
+                                 mha_dtype dt, mha_dtype out_dt, cudaStream_t stream) {
   if (M == 0) return cudaSuccess;
+  if (dt == MHA_BF16 && out_dt == MHA_F32)
+    return launch_bf16_to_f32(a, b, gamma, beta, eps, out, M, D, stream);
+  if (out_dt != dt) return cudaErrorInvalidValue;
   return dt == MHA_BF16 ? launch_typed<__nv_bfloat16>(a, b, gamma, beta, eps, out, M, D, stream)
                         : launch_typed<float>(a, b, gamma, beta, eps, out, M, D, stream);
 }
