@@ -15,15 +15,20 @@
 // whole rows: the fp32 accumulator holds N of the 512 tensor-memory columns
 // and each epilogue thread owns one row.  The epilogue makes two passes
 // over the row in tensor memory:
-//   1. v = acc + bias + R (R read through a shared-memory transpose so that
-//      each load instruction moves four whole 128-byte row pieces); per
+//   1. v = acc + bias + R (R arrives by TMA, 32 rows x 64 columns per warp
+//      and chunk, in a two-buffer ring whose first chunks load while the
+//      MMAs run; bias, gamma and beta sit in shared memory); per
 //      64-column chunk the mean and the centred sum of squares, merged
 //      chunk by chunk with the pairwise update of Chan, Golub and LeVeque
 //      ("Updating formulae and a pairwise algorithm for computing sample
 //      variances", 1979): no E[v^2] - E[v]^2 cancellation; v goes back into
 //      tensor memory;
 //   2. y = (v - mean) / sqrt(var + eps) * gamma + beta, population variance
-//      (divisor N), stored as bf16 or fp32 through the same transpose.
+//      (divisor N), stored as bf16 or fp32 through a per-warp shared-memory
+//      transpose, so that each store instruction writes four whole 128-byte
+//      row pieces.
+// Row tile t walks its k-steps starting at t mod (K / 64): all CTAs share
+// W, and staggering keeps them from asking the same L2 lines at once.
 // Warp roles and the TMA ring are those of the plain projection kernel:
 // warp 0 TMA producer, warp 1 MMA issuer and TMEM owner, warps 2-5 epilogue.
 // One accumulator: the next tile's MMAs wait for the epilogue, while the TMA
@@ -46,29 +51,42 @@ struct LnCfg {
   static_assert(NB >= 1 && NB <= 8, "N = 64..512");
   static constexpr int N = 64 * NB;
   static constexpr int kStageBytes = kABytes + NB * kWBox;
-  static constexpr int kStages = 4 * kStageBytes <= 196608 ? 4 : 3 * kStageBytes <= 196608 ? 3 : 2;
+  // residual ring per epilogue warp: kRB buffers of 32 rows x 64 columns
+  static constexpr int kRB = 2;
+  // operand stages: as many as fit beside the residual rings, the output
+  // staging, bias / gamma / beta and the barriers (up to four)
+  static constexpr int kStageBudget =
+      232448 - 1024 - 512 - 4 * kRB * kStageWarpBytes - 4 * kStageWarpBytes - 3 * N * 2;
+  static constexpr int kStages = kStageBudget / kStageBytes >= 4 ? 4 : kStageBudget / kStageBytes;
+  static_assert(kStages >= 2, "operand stages");
   static constexpr uint32_t kTmemCols = N <= 64 ? 64u : N <= 128 ? 128u : N <= 256 ? 256u : 512u;
   // MMA column chunks of at most 256 (the largest N of one M = 128 MMA)
   static constexpr int kChunks = (N + 255) / 256;
   __host__ __device__ static constexpr int chunk_n(int c) { return N - 256 * c < 256 ? N - 256 * c : 256; }
-  // barriers: full[S], empty[S], acc_full, acc_empty, drain
+  // barriers: full[S], empty[S], acc_full, acc_empty, drain, residual[4][kRB]
   __host__ __device__ static constexpr int bFull(int s) { return s; }
   __host__ __device__ static constexpr int bEmpty(int s) { return kStages + s; }
   static constexpr int bAccFull = 2 * kStages;
   static constexpr int bAccEmpty = 2 * kStages + 1;
   static constexpr int bDrain = 2 * kStages + 2;
-  static constexpr int kNumBars = 2 * kStages + 3;
-  static constexpr int kOffBar = kStages * kStageBytes;
+  __host__ __device__ static constexpr int bRes(int w, int b) { return 2 * kStages + 3 + w * kRB + b; }
+  static constexpr int kNumBars = 2 * kStages + 3 + 4 * kRB;
+  // shared memory from a 1024-byte aligned base: stages, residual rings
+  // (1024-byte aligned: the TMA's 128-byte swizzle), output staging,
+  // bias / gamma / beta, barriers, misc
+  static constexpr int kOffRes = kStages * kStageBytes;
+  static constexpr int kOffStage = kOffRes + 4 * kRB * kStageWarpBytes;
+  static constexpr int kOffVec = kOffStage + 4 * kStageWarpBytes;
+  static constexpr int kOffBar = kOffVec + 3 * N * 2;
   static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
-  static constexpr int kOffStage = (kOffMisc + 16 + 127) & ~127;
-  static constexpr int kSmemBytes = kOffStage + 4 * kStageWarpBytes + 1024;
+  static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
   static_assert(kSmemBytes <= 232448, "shared memory");
 };
 
 struct GemmLnParams {
   void* C;                          // [M, N], bf16 or fp32
   const __nv_bfloat16* bias;        // [N]
-  const __nv_bfloat16* resid;       // [M, N]
+  const __nv_bfloat16* resid;       // [M, N] (read through its tensor map)
   const __nv_bfloat16* gamma;       // [N]
   const __nv_bfloat16* beta;        // [N]
   float eps;
@@ -86,13 +104,18 @@ __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, uint64
   }
 }
 
+__device__ __forceinline__ void fence_proxy_async_shared() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
 template <int NB>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_ln_bf16_kernel(const __grid_constant__ CUtensorMap tA,
-                        const __grid_constant__ CUtensorMap tW, const GemmLnParams p) {
+                        const __grid_constant__ CUtensorMap tW,
+                        const __grid_constant__ CUtensorMap tR, const GemmLnParams p) {
   using C = LnCfg<NB>;
   constexpr int N = C::N;
   extern __shared__ uint8_t smem_raw[];
@@ -114,6 +137,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(C::bAccFull), 1);
     mbar_init(bar(C::bAccEmpty), 128);
     mbar_init(bar(C::bDrain), 1);
+    for (int w = 0; w < 4; ++w)
+      for (int b = 0; b < C::kRB; ++b) mbar_init(bar(C::bRes(w, b)), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -124,6 +149,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tA);
     tma_prefetch_desc(&tW);
+    tma_prefetch_desc(&tR);
+  }
+  if (warp >= 2) {
+    // bias, gamma and beta for every tile of this CTA, in shared memory
+    uint4* vec = reinterpret_cast<uint4*>(gbase + C::kOffVec);
+    for (int i = threadIdx.x - 64; i < 3 * N / 8; i += 128) {
+      const int which = i / (N / 8), piece = i - which * (N / 8);
+      const __nv_bfloat16* src = which == 0 ? p.bias : which == 1 ? p.gamma : p.beta;
+      vec[i] = __ldg(reinterpret_cast<const uint4*>(src) + piece);
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -140,13 +175,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kt = 0; kt < num_k; ++kt, ++g) {
           const int st = g % C::kStages;
           const uint32_t ph = (g / C::kStages) & 1;
+          // Row tile t starts its k walk at k-step t mod num_k: the CTAs
+          // running at once then read different rows of W, instead of all of
+          // them asking the same L2 lines for the same k-step at once.
+          const int kk = (kt + t) % num_k;
           if (!(ok = mbar_wait(bar(C::bEmpty(st)), ph ^ 1u, ctl))) break;
           const uint32_t sa = base + st * C::kStageBytes;
           mbar_expect_tx(bar(C::bFull(st)), C::kStageBytes);
-          tma_load_2d(sa, &tA, bar(C::bFull(st)), kt * kBK, m0);
+          tma_load_2d(sa, &tA, bar(C::bFull(st)), kk * kBK, m0);
 #pragma unroll
           for (int nb = 0; nb < NB; ++nb)
-            tma_load_2d(sa + kABytes + nb * kWBox, &tW, bar(C::bFull(st)), nb * 64, kt * kBK);
+            tma_load_2d(sa + kABytes + nb * kWBox, &tW, bar(C::bFull(st)), nb * 64, kk * kBK);
         }
       }
       for (int q = max(0, g - C::kStages); q < g; ++q)
@@ -189,12 +228,36 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // epilogue: warp w may touch TMEM lanes [32 (w % 4), 32 (w % 4) + 32)
     const int quarter = warp & 3;
+    const int ew = warp - 2;  // epilogue warp 0..3: its residual ring and staging
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    uint4* stg = reinterpret_cast<uint4*>(gbase + C::kOffStage + (warp - 2) * kStageWarpBytes);
-    const int q = lane & 7;  // the 16-byte piece this lane moves in the transposes
+    uint4* stg = reinterpret_cast<uint4*>(gbase + C::kOffStage + ew * kStageWarpBytes);
+    const uint4* vec = reinterpret_cast<const uint4*>(gbase + C::kOffVec);
+    const uint32_t res_base = base + C::kOffRes + ew * C::kRB * kStageWarpBytes;
+    const uint4* res = reinterpret_cast<const uint4*>(gbase + C::kOffRes +
+                                                      ew * C::kRB * kStageWarpBytes);
+    const int q = lane & 7;  // the 16-byte piece this lane moves in the store transpose
+    // The warp's residual rows (32 rows x 64 columns per chunk) arrive by TMA
+    // in a ring of kRB buffers, 128-byte swizzled: 16-byte piece qq of row r
+    // at slot qq ^ (r & 7).  Chunk g of this warp (counted across tiles)
+    // uses buffer g % kRB with phase (g / kRB) & 1.
+    int g_issue = 0, g_use = 0;
+    auto issue_res = [&](int t_next, int cb) {
+      if (lane == 0) {
+        const int b = g_issue % C::kRB;
+        fence_proxy_async_shared();  // the warp's reads of this buffer came first
+        mbar_expect_tx(bar(C::bRes(ew, b)), kStageWarpBytes);
+        tma_load_2d(res_base + b * kStageWarpBytes, &tR, bar(C::bRes(ew, b)), cb * 64,
+                    t_next * kBM + quarter * 32);
+      }
+      ++g_issue;
+    };
+    const int first = blockIdx.x;
+    if (first < p.mt)
+      for (int cb = 0; cb < C::kRB && cb < NB; ++cb) issue_res(first, cb);
     int i = 0;
-    for (int t = blockIdx.x; t < p.mt; t += gridDim.x, ++i) {
-      const bool ok = num_k > 0 && mbar_wait_warp(bar(C::bAccFull), i & 1, ctl);
+    bool ok = true;
+    for (int t = first; t < p.mt; t += gridDim.x, ++i) {
+      ok = num_k > 0 && mbar_wait_warp(bar(C::bAccFull), i & 1, ctl);
       if (!ok) break;
       tc_fence_after();
       const int row0 = t * kBM + quarter * 32;  // this warp's first row
@@ -206,27 +269,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t v[64];
         tmem_ld32(lane_base + n, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
         tmem_ld32(lane_base + n + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
-        // the warp's 32 residual rows, 64 columns: lane l loads piece l % 8
-        // of row 4 g4 + l / 8 (four whole 128-byte row pieces per
-        // instruction); piece qq of row r sits at slot qq ^ (r & 7)
-#pragma unroll
-        for (int g4 = 0; g4 < 8; ++g4) {
-          const int rr = 4 * g4 + (lane >> 3);
-          uint4 w = make_uint4(0u, 0u, 0u, 0u);
-          if (row0 + rr < p.M)
-            w = __ldg(reinterpret_cast<const uint4*>(p.resid + static_cast<size_t>(row0 + rr) * N +
-                                                     n) + q);
-          stg[rr * 8 + (q ^ (rr & 7))] = w;
-        }
-        __syncwarp();
+        const int b = g_use % C::kRB;
+        ok = mbar_wait_warp(bar(C::bRes(ew, b)), (g_use / C::kRB) & 1, ctl);
+        ++g_use;
         tmem_ld_wait(v);
+        if (!ok) break;
+        const uint4* rb = res + b * (kStageWarpBytes / 16);
         float s = 0.f;
 #pragma unroll
         for (int qq = 0; qq < 8; ++qq) {
-          const uint4 r = stg[lane * 8 + (qq ^ (lane & 7))];
-          const uint4 b = __ldg(reinterpret_cast<const uint4*>(p.bias + n) + qq);
+          const uint4 r = rb[lane * 8 + (qq ^ (lane & 7))];
+          const uint4 bi = vec[n / 8 + qq];
           const uint32_t rw[4] = {r.x, r.y, r.z, r.w};
-          const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
+          const uint32_t bw[4] = {bi.x, bi.y, bi.z, bi.w};
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const float lo = __uint_as_float(v[8 * qq + 2 * k]) + bf16_lo(bw[k]) + bf16_lo(rw[k]);
@@ -237,7 +292,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             s += lo + hi;
           }
         }
-        __syncwarp();  // the staging rows are rewritten by the next chunk
+        __syncwarp();  // every lane has read the buffer before it is refilled
+        if (cb + C::kRB < NB) issue_res(t, cb + C::kRB);
         // this chunk's mean and centred sum of squares, then the pairwise merge
         const float mc = s * (1.f / 64.f);
         float qc = 0.f;
@@ -258,7 +314,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st32(lane_base + n, *reinterpret_cast<const uint32_t(*)[32]>(&v[0]));
         tmem_st32(lane_base + n + 32, *reinterpret_cast<const uint32_t(*)[32]>(&v[32]));
       }
+      if (!ok) break;
       tmem_st_wait();
+      // the next tile's first residual chunks load while this one finishes
+      if (t + static_cast<int>(gridDim.x) < p.mt)
+        for (int cb = 0; cb < C::kRB && cb < NB; ++cb) issue_res(t + gridDim.x, cb);
       const float inv = 1.f / sqrtf(m2 * (1.f / static_cast<float>(N)) + p.eps);
       // ---- pass 2: y = (v - mean) * inv * gamma + beta, stored row-major
 #pragma unroll 1
@@ -270,8 +330,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld_wait(v);
 #pragma unroll
         for (int qq = 0; qq < 8; ++qq) {
-          const uint4 gv = __ldg(reinterpret_cast<const uint4*>(p.gamma + n) + qq);
-          const uint4 bv = __ldg(reinterpret_cast<const uint4*>(p.beta + n) + qq);
+          const uint4 gv = vec[N / 8 + n / 8 + qq];
+          const uint4 bv = vec[2 * (N / 8) + n / 8 + qq];
           const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
           const uint32_t bw[4] = {bv.x, bv.y, bv.z, bv.w};
 #pragma unroll
@@ -330,6 +390,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(bar(C::bAccEmpty));
     }
+    // every residual copy this warp issued lands before the CTA exits
+    for (int g = max(0, g_issue - C::kRB); g < g_issue; ++g)
+      if (lane == 0) wait_drain(bar(C::bRes(ew, g % C::kRB)), (g / C::kRB) & 1, p.limit_ns);
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -349,7 +413,7 @@ int current_sm_count() {
 template <int NB>
 cudaError_t launch_nb(const GemmLnArgs& g, const DeviceCtl& ctl) {
   using C = LnCfg<NB>;
-  CUtensorMap ta, tw;
+  CUtensorMap ta, tw, tr;
   const uint64_t adims[2] = {static_cast<uint64_t>(g.K), static_cast<uint64_t>(g.M)};
   const uint64_t astr[1] = {static_cast<uint64_t>(g.K) * 2};
   const uint32_t abox[2] = {64, 128};
@@ -360,6 +424,13 @@ cudaError_t launch_nb(const GemmLnArgs& g, const DeviceCtl& ctl) {
                          astr, abox, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_tensor_map(&tw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(g.W), wdims,
                          wstr, wbox, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  // the residual [M, N]: 32-row x 64-column boxes (one epilogue warp's chunk)
+  const uint64_t rdims[2] = {static_cast<uint64_t>(C::N), static_cast<uint64_t>(g.M)};
+  const uint64_t rstr[1] = {static_cast<uint64_t>(C::N) * 2};
+  const uint32_t rbox[2] = {64, 32};
+  if (!encode_tensor_map(&tr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(g.resid),
+                         rdims, rstr, rbox, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   GemmLnParams p{};
   p.C = g.C;
@@ -381,7 +452,7 @@ cudaError_t launch_nb(const GemmLnArgs& g, const DeviceCtl& ctl) {
   // one CTA per SM at most (tensor memory and shared memory admit no second)
   const int sms = current_sm_count();
   const int grid = p.mt < sms ? p.mt : sms;
-  kern<<<grid, kThreads, C::kSmemBytes, g.stream>>>(ta, tw, p);
+  kern<<<grid, kThreads, C::kSmemBytes, g.stream>>>(ta, tw, tr, p);
   return cudaGetLastError();
 }
 
