@@ -59,6 +59,12 @@ CASES = [
     (torch.float32, 8, 512, 512, 256, 4, NONE, None, False),
     (torch.float32, 4, 300, 300, 90, 3, NONE, None, False),
     (torch.float32, 3, 50, 70, 90, 3, PAD, [70, 1, 33], True),
+    # fp32 self-attention: key padding with a length of 1, causal + padding,
+    # 512 rows, d = 128
+    (torch.float32, 4, 100, 100, 256, 4, PAD, [100, 1, 57, 99], False),
+    (torch.float32, 3, 64, 64, 192, 6, PAD | CAUSAL, [64, 7, 33], False),
+    (torch.float32, 2, 256, 256, 384, 6, CAUSAL, None, False),
+    (torch.float32, 1, 200, 200, 512, 4, NONE, None, False),
 ]
 
 
