@@ -52,6 +52,11 @@ CASES = [
     (torch.bfloat16, 1, 100, 384, 6, 1536, mha.MASK_NONE, None),
     # d_model 1024: the seven-launch form (residual + LayerNorm as own launches)
     (torch.bfloat16, 2, 96, 1024, 8, 1024, mha.MASK_CAUSAL, None),
+    # more 128-row tiles than SMs: CTAs of the fused epilogue GEMMs take a
+    # second tile (the accumulator handed back, the next tile's residual
+    # prefetched); 20480 and 19968 rows, d_model 256 and 512
+    (torch.bfloat16, 128, 160, 256, 4, 512, mha.MASK_NONE, None),
+    (torch.bfloat16, 48, 416, 512, 8, 1024, mha.MASK_KEY_PADDING, [200 + 4 * i for i in range(48)]),
     (torch.float32, 1, 128, 512, 8, 2048, mha.MASK_NONE, None),
     (torch.float32, 2, 50, 96, 3, 200, mha.MASK_CAUSAL, None),
 ]
