@@ -11,10 +11,14 @@
 //
 // CTA tile 128 x 256, k-step 64, a 4-stage TMA ring.  A (activations) is
 // K-major; W is row-major [K, N], i.e. MN-major for the MMA's B operand, and
-// is loaded as 64 x 64 boxes (64 N-columns of 128 bytes, 64 K-rows).
-// Warp roles: warp 0 TMA producer, warp 1 MMA issuer and TMEM owner,
-// warps 2-5 epilogue (TMEM -> registers, one row per thread; then through
-// a shared-memory transpose so that every store instruction writes whole
+// is loaded as four 64 x 64 blocks (64 N-columns of 128 bytes, 64 K-rows)
+// by one copy: the tensor map views W as [N/64][K][64], so the box lands as
+// the four blocks in a row.  (Each copy instruction costs the producer
+// thread about 100 cycles; five per stage would take as long as the stage's
+// MMAs.)  Warp roles: warp 0 TMA producer, warp 1 MMA issuer and TMEM
+// owner, warps 2-9 epilogue, two per TMEM lane quarter, each half of the
+// columns (TMEM -> registers, one row per thread; then through a
+// shared-memory transpose so that every store instruction writes whole
 // 128-byte row segments).
 // Up to three problems of one shape share a launch, which is how the Q, K
 // and V projections of self-attention run as one launch.
@@ -38,7 +42,8 @@ constexpr int kABytes = kBM * kBK * 2;           // 16 KB
 constexpr int kWBox = 64 * 64 * 2;               // 8 KB: one 64(N) x 64(K) box
 constexpr int kWBytes = kBK * kBN * 2;           // 32 KB
 constexpr int kStageBytes = kABytes + kWBytes;   // 48 KB
-constexpr int kThreads = 192;
+constexpr int kEpiWarps = 8;   // two per TMEM lane quarter, each half of the 256 columns
+constexpr int kThreads = 32 * (2 + kEpiWarps);
 constexpr uint32_t kTmemCols = 512;   // two kBN-column accumulators
 // barriers: full[kStages], empty[kStages], acc_full[2], acc_empty[2], drain
 __host__ __device__ constexpr int bFull(int s) { return s; }
@@ -52,7 +57,7 @@ constexpr int kOffMisc = kOffBar + 8 * kNumBars;
 // epilogue staging: per epilogue warp, 32 rows x 128 bytes (64 bf16 columns)
 constexpr int kOffStage = (kOffMisc + 16 + 127) & ~127;
 constexpr int kStageWarpBytes = 32 * 128;
-constexpr int kSmemBytes = kOffStage + 4 * kStageWarpBytes + 1024;
+constexpr int kSmemBytes = kOffStage + kEpiWarps * kStageWarpBytes + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory");
 
 struct GemmParams {
@@ -101,7 +106,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(bAccFull(b)), 1);
-      mbar_init(bar(bAccEmpty(b)), 128);
+      mbar_init(bar(bAccEmpty(b)), 32 * kEpiWarps);
     }
     mbar_init(bar(bDrain), 1);
     *abort_flag = 0;
@@ -152,9 +157,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t sa = base + st * kStageBytes;
           mbar_expect_tx(bar(bFull(st)), kStageBytes);
           tma_load_2d(sa, tA, bar(bFull(st)), kt * kBK, m0);
-#pragma unroll
-          for (int nb = 0; nb < kBN / 64; ++nb)
-            tma_load_2d(sa + kABytes + nb * kWBox, tW, bar(bFull(st)), n0 + nb * 64, kt * kBK);
+          // all four 64 x 64 boxes of W in one copy (W viewed as
+          // [N/64][K][64], so the box lands as four consecutive 8 KB blocks)
+          tma_load_3d(sa + kABytes, tW, bar(bFull(st)), 0, kt * kBK, n0 / 64);
         }
       }
       for (int q = max(0, g - kStages); q < g; ++q)
@@ -193,8 +198,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       wait_drain(bar(bDrain), 0, p.limit_ns);
     }
   } else {
-    // epilogue: warp w may read TMEM lanes [32*(w%4), 32*(w%4)+32)
+    // epilogue: warp w may read TMEM lanes [32*(w%4), 32*(w%4)+32); the two
+    // warps of a quarter take the tile's columns [0, 128) and [128, 256)
     const int quarter = warp & 3;
+    const int chalf = (warp - 2) / 4;
     const int row = quarter * 32 + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     int i = 0;
@@ -255,8 +262,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // slot q ^ (r & 7), so that both the row-wise writes and the
       // piece-wise reads take the minimum four 128-byte wavefronts
       uint4* stg = reinterpret_cast<uint4*>(gbase + kOffStage + (warp - 2) * kStageWarpBytes);
-      int cb = 0;
-      for (; cb + 2 <= kBN / 32 && n0 + cb * 32 + 64 <= p.N; cb += 2) {
+      const int cb_end = (chalf + 1) * (kBN / 64);
+      int cb = chalf * (kBN / 64);
+      for (; cb + 2 <= cb_end && n0 + cb * 32 + 64 <= p.N; cb += 2) {
         const int n = n0 + cb * 32;
         uint32_t v[64];
         tmem_ld32(tbase + cb * 32, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
@@ -279,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();  // the staging rows are rewritten by the next pair
       }
       // a trailing 32-column block (N not a multiple of 64): row by row
-      for (; cb < kBN / 32; ++cb) {
+      for (; cb < cb_end; ++cb) {
         const int n = n0 + cb * 32;
         if (n >= p.N) break;  // uniform across the warp
         uint32_t v[32];
@@ -318,6 +326,7 @@ int num_sms() {
 
 cudaError_t launch_gemm_bf16(const GemmArgs& g, const DeviceCtl& ctl) {
   if (g.M == 0 || g.N == 0) return cudaSuccess;
+  if (g.N % 64 != 0) return cudaErrorInvalidValue;  // W is copied in 64-column blocks
   CUtensorMap ta[3], tw[3];
   GemmParams p{};
   for (int i = 0; i < 3; ++i) {
@@ -325,12 +334,13 @@ cudaError_t launch_gemm_bf16(const GemmArgs& g, const DeviceCtl& ctl) {
     const uint64_t adims[2] = {static_cast<uint64_t>(g.K), static_cast<uint64_t>(g.M)};
     const uint64_t astr[1] = {static_cast<uint64_t>(g.K) * 2};
     const uint32_t abox[2] = {64, 128};
-    const uint64_t wdims[2] = {static_cast<uint64_t>(g.N), static_cast<uint64_t>(g.K)};
-    const uint64_t wstr[1] = {static_cast<uint64_t>(g.N) * 2};
-    const uint32_t wbox[2] = {64, 64};
+    // W [K, N] as a 3-D tensor (64 columns, K rows, N/64 column blocks)
+    const uint64_t wdims[3] = {64, static_cast<uint64_t>(g.K), static_cast<uint64_t>(g.N) / 64};
+    const uint64_t wstr[2] = {static_cast<uint64_t>(g.N) * 2, 128};
+    const uint32_t wbox[3] = {64, 64, kBN / 64};
     if (!encode_tensor_map(&ta[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(pr.A),
                            adims, astr, abox, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_tensor_map(&tw[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(pr.W),
+        !encode_tensor_map(&tw[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(pr.W),
                            wdims, wstr, wbox, CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
     p.C[i] = pr.C;

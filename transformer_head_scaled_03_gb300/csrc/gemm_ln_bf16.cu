@@ -183,9 +183,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t sa = base + st * C::kStageBytes;
           mbar_expect_tx(bar(C::bFull(st)), C::kStageBytes);
           tma_load_2d(sa, &tA, bar(C::bFull(st)), kk * kBK, m0);
-#pragma unroll
-          for (int nb = 0; nb < NB; ++nb)
-            tma_load_2d(sa + kABytes + nb * kWBox, &tW, bar(C::bFull(st)), nb * 64, kk * kBK);
+          // all NB 64 x 64 blocks of W in one copy (W viewed as [NB][K][64])
+          tma_load_3d(sa + kABytes, &tW, bar(C::bFull(st)), 0, kk * kBK, 0);
         }
       }
       for (int q = max(0, g - C::kStages); q < g; ++q)
@@ -417,12 +416,14 @@ cudaError_t launch_nb(const GemmLnArgs& g, const DeviceCtl& ctl) {
   const uint64_t adims[2] = {static_cast<uint64_t>(g.K), static_cast<uint64_t>(g.M)};
   const uint64_t astr[1] = {static_cast<uint64_t>(g.K) * 2};
   const uint32_t abox[2] = {64, 128};
-  const uint64_t wdims[2] = {static_cast<uint64_t>(C::N), static_cast<uint64_t>(g.K)};
-  const uint64_t wstr[1] = {static_cast<uint64_t>(C::N) * 2};
-  const uint32_t wbox[2] = {64, 64};
+  // W [K, N] as a 3-D tensor (64 columns, K rows, NB column blocks): one
+  // copy per stage brings all NB blocks
+  const uint64_t wdims[3] = {64, static_cast<uint64_t>(g.K), static_cast<uint64_t>(NB)};
+  const uint64_t wstr[2] = {static_cast<uint64_t>(C::N) * 2, 128};
+  const uint32_t wbox[3] = {64, 64, NB};
   if (!encode_tensor_map(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(g.A), adims,
                          astr, abox, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_tensor_map(&tw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(g.W), wdims,
+      !encode_tensor_map(&tw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(g.W), wdims,
                          wstr, wbox, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   // the residual [M, N]: 32-row x 64-column boxes (one epilogue warp's chunk)
