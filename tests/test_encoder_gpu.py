@@ -57,6 +57,11 @@ CASES = [
     # prefetched); 20480 and 19968 rows, d_model 256 and 512
     (torch.bfloat16, 128, 160, 256, 4, 512, mha.MASK_NONE, None),
     (torch.bfloat16, 48, 416, 512, 8, 1024, mha.MASK_KEY_PADDING, [200 + 4 * i for i in range(48)]),
+    # d_model 320 and 192 (an odd number of 64-column blocks): the fused
+    # epilogue GEMMs in their single-CTA form (even counts run as CTA pairs),
+    # the second with more 128-row tiles than SMs
+    (torch.bfloat16, 2, 150, 320, 5, 640, mha.MASK_CAUSAL, None),
+    (torch.bfloat16, 64, 320, 192, 3, 384, mha.MASK_NONE, None),
     (torch.float32, 1, 128, 512, 8, 2048, mha.MASK_NONE, None),
     (torch.float32, 2, 50, 96, 3, 200, mha.MASK_CAUSAL, None),
 ]

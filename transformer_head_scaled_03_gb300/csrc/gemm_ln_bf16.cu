@@ -35,6 +35,8 @@
 // ring keeps loading ahead.
 #include "internal.h"
 #include "ptx.cuh"
+#include "ptx_cluster.cuh"
+#include "ptx_pair.cuh"
 
 namespace mha {
 namespace {
@@ -43,40 +45,58 @@ constexpr int kBM = 128;
 constexpr int kBK = 64;
 constexpr int kABytes = kBM * kBK * 2;  // 16 KB: 128 rows x 64 k
 constexpr int kWBox = 64 * 64 * 2;      // 8 KB: one 64(N) x 64(K) box of W
-constexpr int kThreads = 192;
-constexpr int kStageWarpBytes = 32 * 128;  // epilogue staging: 32 rows x 128 bytes
+constexpr int kEpiWarps = 8;   // two per TMEM lane quarter, each half of the row's columns
+constexpr int kThreads = 32 * (2 + kEpiWarps);
+constexpr int kStageWarpBytes = 32 * 128;  // one residual / staging buffer: 32 rows x 128 bytes
 
-template <int NB>  // N = 64 * NB output columns = whole rows
+// N = 64 * NB output columns = whole rows.  kPair: the CTA pair form (a
+// cluster of two; M = 256 products issued by the even CTA, each CTA staging
+// its own 128 rows of A and half of every MMA's W columns), which needs every
+// column chunk to split into whole 64-column blocks, i.e. NB even.
+template <int NB, bool kPair>
 struct LnCfg {
   static_assert(NB >= 1 && NB <= 8, "N = 64..512");
+  static_assert(!kPair || NB % 2 == 0, "the pair form splits chunks into 64-column halves");
   static constexpr int N = 64 * NB;
-  static constexpr int kStageBytes = kABytes + NB * kWBox;
+  static constexpr int kTileM = kPair ? 2 * kBM : kBM;   // rows of one tile (both CTAs)
+  static constexpr int kWBlocks = kPair ? NB / 2 : NB;   // 64-column W blocks this CTA stages
+  // W blocks per copy in the pair form: a chunk's half is two blocks when
+  // every chunk is 256 columns wide (NB a multiple of 4), else one per copy
+  static constexpr int kPB = kPair ? (NB % 4 == 0 ? 2 : 1) : NB;
+  static constexpr int kStageBytes = kABytes + kWBlocks * kWBox;
   // residual ring per epilogue warp: kRB buffers of 32 rows x 64 columns
   static constexpr int kRB = 2;
-  // operand stages: as many as fit beside the residual rings, the output
-  // staging, bias / gamma / beta and the barriers (up to four)
+  // operand stages: as many as fit beside the residual rings (which also
+  // stage the output), bias / gamma / beta, the statistics exchange and the
+  // barriers (up to four)
+  static constexpr int kStatBytes = 4 * 2 * 32 * 8 + 4 * 2 * 4;  // (mean, m2) per row, verdicts
   static constexpr int kStageBudget =
-      232448 - 1024 - 512 - 4 * kRB * kStageWarpBytes - 4 * kStageWarpBytes - 3 * N * 2;
+      232448 - 1024 - 512 - kEpiWarps * kRB * kStageWarpBytes - 3 * N * 2 - kStatBytes;
   static constexpr int kStages = kStageBudget / kStageBytes >= 4 ? 4 : kStageBudget / kStageBytes;
   static_assert(kStages >= 2, "operand stages");
   static constexpr uint32_t kTmemCols = N <= 64 ? 64u : N <= 128 ? 128u : N <= 256 ? 256u : 512u;
   // MMA column chunks of at most 256 (the largest N of one M = 128 MMA)
   static constexpr int kChunks = (N + 255) / 256;
   __host__ __device__ static constexpr int chunk_n(int c) { return N - 256 * c < 256 ? N - 256 * c : 256; }
-  // barriers: full[S], empty[S], acc_full, acc_empty, drain, residual[4][kRB]
+  // barriers: full[S], empty[S], acc_full, acc_empty, drain, residual[kEpiWarps][kRB]
   __host__ __device__ static constexpr int bFull(int s) { return s; }
   __host__ __device__ static constexpr int bEmpty(int s) { return kStages + s; }
   static constexpr int bAccFull = 2 * kStages;
   static constexpr int bAccEmpty = 2 * kStages + 1;
   static constexpr int bDrain = 2 * kStages + 2;
   __host__ __device__ static constexpr int bRes(int w, int b) { return 2 * kStages + 3 + w * kRB + b; }
-  static constexpr int kNumBars = 2 * kStages + 3 + 4 * kRB;
+  static constexpr int kNumBars = 2 * kStages + 3 + kEpiWarps * kRB;
+  // acc_empty arrivals: one per epilogue warp of each CTA of the tile
+  static constexpr int kAccArrivals = kPair ? 2 * kEpiWarps : kEpiWarps;
+  // the two epilogue warps of a lane quarter split the row's NB chunks
+  __host__ __device__ static constexpr int cb_begin(int chalf) { return chalf ? (NB + 1) / 2 : 0; }
+  __host__ __device__ static constexpr int cb_end(int chalf) { return chalf ? NB : (NB + 1) / 2; }
   // shared memory from a 1024-byte aligned base: stages, residual rings
   // (1024-byte aligned: the TMA's 128-byte swizzle), output staging,
   // bias / gamma / beta, barriers, misc
   static constexpr int kOffRes = kStages * kStageBytes;
-  static constexpr int kOffStage = kOffRes + 4 * kRB * kStageWarpBytes;
-  static constexpr int kOffVec = kOffStage + 4 * kStageWarpBytes;
+  static constexpr int kOffStat = kOffRes + kEpiWarps * kRB * kStageWarpBytes;
+  static constexpr int kOffVec = kOffStat + kStatBytes;
   static constexpr int kOffBar = kOffVec + 3 * N * 2;
   static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
@@ -108,15 +128,20 @@ __device__ __forceinline__ void fence_proxy_async_shared() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Barrier `id` (1..15) among `count` threads (whole warps).
+__device__ __forceinline__ void named_barrier_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-template <int NB>
+template <int NB, bool kPair>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_ln_bf16_kernel(const __grid_constant__ CUtensorMap tA,
                         const __grid_constant__ CUtensorMap tW,
                         const __grid_constant__ CUtensorMap tR, const GemmLnParams p) {
-  using C = LnCfg<NB>;
+  using C = LnCfg<NB, kPair>;
   constexpr int N = C::N;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -128,6 +153,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const WaitCtl ctl{abort_flag, p.err, p.limit_ns};
+  // tiles of kTileM rows: one per CTA, or in the pair form one per cluster
+  // of two, whose rank-0 CTA issues the MMAs and owns the barriers that
+  // gather both CTAs' stage bytes and both epilogues' releases
+  const uint32_t rank = kPair ? cluster_ctarank() : 0u;
+  const int tile0 = kPair ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int tstride = kPair ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+  auto row_base = [&](int t) { return t * C::kTileM + static_cast<int>(rank) * kBM; };
+  auto lead_bar = [&](int i) -> uint32_t { return kPair ? cluster_map(bar(i), 0u) : bar(i); };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
@@ -135,16 +168,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(C::bEmpty(s)), 1);
     }
     mbar_init(bar(C::bAccFull), 1);
-    mbar_init(bar(C::bAccEmpty), 128);
+    mbar_init(bar(C::bAccEmpty), C::kAccArrivals);
     mbar_init(bar(C::bDrain), 1);
-    for (int w = 0; w < 4; ++w)
+    for (int w = 0; w < kEpiWarps; ++w)
       for (int b = 0; b < C::kRB; ++b) mbar_init(bar(C::bRes(w, b)), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc<C::kTmemCols>(smem_u32(tmem_slot));
-    tmem_relinquish();
+    if constexpr (kPair) {
+      tmem_alloc_pair<C::kTmemCols>(smem_u32(tmem_slot));
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc<C::kTmemCols>(smem_u32(tmem_slot));
+      tmem_relinquish();
+    }
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tA);
@@ -154,14 +192,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp >= 2) {
     // bias, gamma and beta for every tile of this CTA, in shared memory
     uint4* vec = reinterpret_cast<uint4*>(gbase + C::kOffVec);
-    for (int i = threadIdx.x - 64; i < 3 * N / 8; i += 128) {
+    for (int i = threadIdx.x - 64; i < 3 * N / 8; i += 32 * kEpiWarps) {
       const int which = i / (N / 8), piece = i - which * (N / 8);
       const __nv_bfloat16* src = which == 0 ? p.bias : which == 1 ? p.gamma : p.beta;
       vec[i] = __ldg(reinterpret_cast<const uint4*>(src) + piece);
     }
   }
   tc_fence_before();
-  __syncthreads();
+  if constexpr (kPair) {
+    // both CTAs' barriers and tensor memory exist before either touches the other's
+    __syncthreads();
+    cluster_sync();
+  } else {
+    __syncthreads();
+  }
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
   const int num_k = (p.K + kBK - 1) / kBK;
@@ -170,8 +214,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       int g = 0;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < p.mt; t += gridDim.x) {
-        const int m0 = t * kBM;
+      for (int t = tile0; ok && t < p.mt; t += tstride) {
+        const int m0 = row_base(t);
         for (int kt = 0; kt < num_k; ++kt, ++g) {
           const int st = g % C::kStages;
           const uint32_t ph = (g / C::kStages) & 1;
@@ -181,22 +225,43 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int kk = (kt + t) % num_k;
           if (!(ok = mbar_wait(bar(C::bEmpty(st)), ph ^ 1u, ctl))) break;
           const uint32_t sa = base + st * C::kStageBytes;
-          mbar_expect_tx(bar(C::bFull(st)), C::kStageBytes);
-          tma_load_2d(sa, &tA, bar(C::bFull(st)), kk * kBK, m0);
-          // all NB 64 x 64 blocks of W in one copy (W viewed as [NB][K][64])
-          tma_load_3d(sa + kABytes, &tW, bar(C::bFull(st)), 0, kk * kBK, 0);
+          if constexpr (kPair) {
+            // this CTA's rows of A and its half of each chunk's W columns
+            // (chunk c covers blocks 4c.. of W; rank r takes the r-th half),
+            // all reported to rank 0's full barrier
+            if (rank == 0) mbar_expect_tx(bar(C::bFull(st)), 2 * C::kStageBytes);
+            const uint32_t full = lead_bar(C::bFull(st));
+            tma_load_2d_pair(sa, &tA, full, kk * kBK, m0);
+#pragma unroll
+            for (int c = 0; c < C::kChunks; ++c) {
+              const int half = C::chunk_n(c) / 128;  // blocks per CTA in chunk c
+#pragma unroll
+              for (int u = 0; u < half / C::kPB; ++u)
+                tma_load_3d_pair(sa + kABytes + (2 * c + u * C::kPB) * kWBox, &tW, full, 0,
+                                 kk * kBK, 4 * c + static_cast<int>(rank) * half + u * C::kPB);
+            }
+          } else {
+            mbar_expect_tx(bar(C::bFull(st)), C::kStageBytes);
+            tma_load_2d(sa, &tA, bar(C::bFull(st)), kk * kBK, m0);
+            // all NB 64 x 64 blocks of W in one copy (W viewed as [NB][K][64])
+            tma_load_3d(sa + kABytes, &tW, bar(C::bFull(st)), 0, kk * kBK, 0);
+          }
         }
       }
-      for (int q = max(0, g - C::kStages); q < g; ++q)
-        wait_drain(bar(C::bFull(q % C::kStages)), (q / C::kStages) & 1, p.limit_ns);
+      if (rank == 0)
+        for (int q = max(0, g - C::kStages); q < g; ++q)
+          wait_drain(bar(C::bFull(q % C::kStages)), (q / C::kStages) & 1, p.limit_ns);
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    if (lane == 0 && rank == 0) {
       int g = 0, i = 0;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < p.mt; t += gridDim.x, ++i) {
-        // the single accumulator, once the epilogue has drained the last tile
-        if (!(ok = mbar_wait(bar(C::bAccEmpty), (i & 1) ^ 1u, ctl))) break;
+      for (int t = tile0; ok && t < p.mt; t += tstride, ++i) {
+        // the single accumulator, once the epilogue (both CTAs' in the pair
+        // form) has drained the last tile
+        if (!(ok = kPair ? mbar_wait_cluster(bar(C::bAccEmpty), (i & 1) ^ 1u, ctl)
+                         : mbar_wait(bar(C::bAccEmpty), (i & 1) ^ 1u, ctl)))
+          break;
         tc_fence_after();
         for (int kt = 0; kt < num_k; ++kt, ++g) {
           const int st = g % C::kStages;
@@ -210,30 +275,56 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int c = 0; c < C::kChunks; ++c) {
               // A: K-major, +32 bytes per 16 k; W: MN-major, +16 rows of 128
-              // bytes per 16 k, 64-column boxes kWBox apart
-              umma_ss(tmem + static_cast<uint32_t>(256 * c), sdesc_sw128(sa + ks * 32, 16, 1024),
-                      sdesc_sw128(sw + c * 4 * kWBox + ks * 16 * 128, kWBox, 1024),
-                      idesc_bf16_f32(kBM, C::chunk_n(c), false, true),
-                      (kt > 0 || ks > 0) ? 1u : 0u);
+              // bytes per 16 k, 64-column boxes kWBox apart (the pair form
+              // stages half of each chunk: 2 blocks per chunk)
+              const uint64_t da = sdesc_sw128(sa + ks * 32, 16, 1024);
+              const uint32_t acc = tmem + static_cast<uint32_t>(256 * c);
+              const uint32_t accum = (kt > 0 || ks > 0) ? 1u : 0u;
+              if constexpr (kPair)
+                umma_ss_pair(acc, da, sdesc_sw128(sw + c * 2 * kWBox + ks * 16 * 128, kWBox, 1024),
+                             idesc_bf16_f32(C::kTileM, C::chunk_n(c), false, true), accum);
+              else
+                umma_ss(acc, da, sdesc_sw128(sw + c * 4 * kWBox + ks * 16 * 128, kWBox, 1024),
+                        idesc_bf16_f32(kBM, C::chunk_n(c), false, true), accum);
             }
           }
-          umma_commit(bar(C::bEmpty(st)));
+          if constexpr (kPair)
+            umma_commit_pair_mc(bar(C::bEmpty(st)), 0x3);  // the stage is free in both CTAs
+          else
+            umma_commit(bar(C::bEmpty(st)));
         }
-        if (ok) umma_commit(bar(C::bAccFull));
+        if (ok) {
+          if constexpr (kPair)
+            umma_commit_pair_mc(bar(C::bAccFull), 0x3);
+          else
+            umma_commit(bar(C::bAccFull));
+        }
       }
-      umma_commit(bar(C::bDrain));
+      if constexpr (kPair)
+        umma_commit_pair(bar(C::bDrain));
+      else
+        umma_commit(bar(C::bDrain));
       wait_drain(bar(C::bDrain), 0, p.limit_ns);
     }
   } else {
-    // epilogue: warp w may touch TMEM lanes [32 (w % 4), 32 (w % 4) + 32)
+    // epilogue: warp w may touch TMEM lanes [32 (w % 4), 32 (w % 4) + 32); the
+    // two warps of a quarter (chalf 0 and 1) take the row's 64-column chunks
+    // [cb_begin, cb_end) each, and merge their row statistics through shared
+    // memory before the second pass
     const int quarter = warp & 3;
-    const int ew = warp - 2;  // epilogue warp 0..3: its residual ring and staging
+    const int ew = warp - 2;          // epilogue warp 0..7: its residual ring
+    const int chalf = ew >> 2;
+    const int cb0 = C::cb_begin(chalf), cb1 = C::cb_end(chalf);
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    uint4* stg = reinterpret_cast<uint4*>(gbase + C::kOffStage + ew * kStageWarpBytes);
     const uint4* vec = reinterpret_cast<const uint4*>(gbase + C::kOffVec);
     const uint32_t res_base = base + C::kOffRes + ew * C::kRB * kStageWarpBytes;
     const uint4* res = reinterpret_cast<const uint4*>(gbase + C::kOffRes +
                                                       ew * C::kRB * kStageWarpBytes);
+    // pass 2 stages its output in the warp's first residual buffer: every
+    // residual chunk of the tile has been read by then
+    uint4* stg = reinterpret_cast<uint4*>(gbase + C::kOffRes + ew * C::kRB * kStageWarpBytes);
+    float2* stat = reinterpret_cast<float2*>(gbase + C::kOffStat);  // [quarter][chalf][lane]
+    volatile int* verdict = reinterpret_cast<volatile int*>(gbase + C::kOffStat + 4 * 2 * 32 * 8);
     const int q = lane & 7;  // the 16-byte piece this lane moves in the store transpose
     // The warp's residual rows (32 rows x 64 columns per chunk) arrive by TMA
     // in a ring of kRB buffers, 128-byte swizzled: 16-byte piece qq of row r
@@ -246,24 +337,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_shared();  // the warp's reads of this buffer came first
         mbar_expect_tx(bar(C::bRes(ew, b)), kStageWarpBytes);
         tma_load_2d(res_base + b * kStageWarpBytes, &tR, bar(C::bRes(ew, b)), cb * 64,
-                    t_next * kBM + quarter * 32);
+                    row_base(t_next) + quarter * 32);
       }
       ++g_issue;
     };
-    const int first = blockIdx.x;
+    const int first = tile0;
     if (first < p.mt)
-      for (int cb = 0; cb < C::kRB && cb < NB; ++cb) issue_res(first, cb);
+      for (int cb = cb0; cb < cb0 + C::kRB && cb < cb1; ++cb) issue_res(first, cb);
     int i = 0;
     bool ok = true;
-    for (int t = first; t < p.mt; t += gridDim.x, ++i) {
+    // Both warps of a quarter take every tile, meet at every statistics
+    // exchange (a warp whose wait failed brings its verdict there) and leave
+    // the loop together, so neither can wait at the exchange for a partner
+    // that has gone.
+    for (int t = first; t < p.mt; t += tstride, ++i) {
       ok = num_k > 0 && mbar_wait_warp(bar(C::bAccFull), i & 1, ctl);
-      if (!ok) break;
       tc_fence_after();
-      const int row0 = t * kBM + quarter * 32;  // this warp's first row
+      const int row0 = row_base(t) + quarter * 32;  // this warp's first row
       // ---- pass 1: v = acc + bias + R, row statistics, v back to TMEM
       float mean = 0.f, m2 = 0.f;
 #pragma unroll 1
-      for (int cb = 0; cb < NB; ++cb) {
+      for (int cb = cb0; ok && cb < cb1; ++cb) {
         const int n = cb * 64;
         uint32_t v[64];
         tmem_ld32(lane_base + n, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
@@ -292,7 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         __syncwarp();  // every lane has read the buffer before it is refilled
-        if (cb + C::kRB < NB) issue_res(t, cb + C::kRB);
+        if (cb + C::kRB < cb1) issue_res(t, cb + C::kRB);
         // this chunk's mean and centred sum of squares, then the pairwise merge
         const float mc = s * (1.f / 64.f);
         float qc = 0.f;
@@ -301,11 +395,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float d = __uint_as_float(v[k]) - mc;
           qc = fmaf(d, d, qc);
         }
-        if (cb == 0) {
+        if (cb == cb0) {
           mean = mc;
           m2 = qc;
         } else {
-          const float na = 64.f * cb, nt = na + 64.f;
+          const float na = 64.f * (cb - cb0), nt = na + 64.f;
           const float delta = mc - mean;
           mean = fmaf(delta, 64.f / nt, mean);
           m2 = m2 + qc + delta * delta * (na * 64.f / nt);
@@ -313,15 +407,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st32(lane_base + n, *reinterpret_cast<const uint32_t(*)[32]>(&v[0]));
         tmem_st32(lane_base + n + 32, *reinterpret_cast<const uint32_t(*)[32]>(&v[32]));
       }
-      if (!ok) break;
+      ok = __all_sync(0xffffffffu, ok);
       tmem_st_wait();
-      // the next tile's first residual chunks load while this one finishes
-      if (t + static_cast<int>(gridDim.x) < p.mt)
-        for (int cb = 0; cb < C::kRB && cb < NB; ++cb) issue_res(t + gridDim.x, cb);
+      // the two halves' statistics, merged in the same order by both warps
+      // of the quarter (so that they normalise with identical values)
+      stat[(quarter * 2 + chalf) * 32 + lane] = make_float2(mean, m2);
+      if (lane == 0) verdict[quarter * 2 + chalf] = ok ? 1 : 0;
+      named_barrier_sync(1 + quarter, 64);
+      const float2 sa = stat[(quarter * 2 + 0) * 32 + lane];
+      const float2 sb = stat[(quarter * 2 + 1) * 32 + lane];
+      const bool both = verdict[quarter * 2] != 0 && verdict[quarter * 2 + 1] != 0;
+      named_barrier_sync(1 + quarter, 64);  // both have read before the next tile writes
+      if (!both) break;
+      {
+        const float na = 64.f * C::cb_end(0), nb = 64.f * (NB - C::cb_end(0));
+        const float delta = sb.x - sa.x;
+        mean = nb > 0.f ? fmaf(delta, nb / static_cast<float>(N), sa.x) : sa.x;
+        m2 = nb > 0.f ? sa.y + sb.y + delta * delta * (na * nb / static_cast<float>(N)) : sa.y;
+      }
       const float inv = 1.f / sqrtf(m2 * (1.f / static_cast<float>(N)) + p.eps);
       // ---- pass 2: y = (v - mean) * inv * gamma + beta, stored row-major
 #pragma unroll 1
-      for (int cb = 0; cb < NB; ++cb) {
+      for (int cb = cb0; cb < cb1; ++cb) {
         const int n = cb * 64;
         uint32_t v[64];
         tmem_ld32(lane_base + n, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
@@ -385,9 +492,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      // the accumulator may take the next tile
+      // the accumulator may take the next tile once every epilogue warp (of
+      // both CTAs in the pair form) has read it
       tc_fence_before();
-      mbar_arrive(bar(C::bAccEmpty));
+      __syncwarp();
+      if (lane == 0) {
+        if constexpr (kPair)
+          mbar_arrive_cluster(lead_bar(C::bAccEmpty));
+        else
+          mbar_arrive(bar(C::bAccEmpty));
+      }
+      // the next tile's first residual chunks load while its MMAs run (the
+      // staging buffer has been read: the __syncwarp above)
+      if (t + tstride < p.mt)
+        for (int cb = cb0; cb < cb0 + C::kRB && cb < cb1; ++cb) issue_res(t + tstride, cb);
     }
     // every residual copy this warp issued lands before the CTA exits
     for (int g = max(0, g_issue - C::kRB); g < g_issue; ++g)
@@ -397,8 +515,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  tc_fence_after();
-  if (warp == 1) tmem_dealloc<C::kTmemCols>(tmem);
+  if constexpr (kPair) {
+    // no CTA of the pair leaves (or frees its tensor memory) while the
+    // other's products, copies or barrier arrivals may still reach it
+    cluster_sync();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc_pair<C::kTmemCols>(tmem);
+  } else {
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc<C::kTmemCols>(tmem);
+  }
 }
 
 int current_sm_count() {
@@ -409,18 +535,55 @@ int current_sm_count() {
   return 1;
 }
 
+// Clusters of two of this kernel that can be resident at once on the current
+// device (each CTA fills an SM, and a cluster sits inside one GPC), asked
+// once per device; half the SM count if the query fails.
+template <int NB>
+int pair_slots() {
+  constexpr int kDevs = 16;
+  static int cache[kDevs];
+  int dev = 0;
+  const int fallback = current_sm_count() / 2 > 0 ? current_sm_count() / 2 : 1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return fallback;
+  if (dev < kDevs && cache[dev] > 0) return cache[dev];
+  using C = LnCfg<NB, true>;
+  auto kern = gemm_ln_bf16_kernel<NB, true>;
+  int n = 0;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) ==
+      cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
+  }
+  cudaGetLastError();
+  if (n <= 0) n = fallback;
+  if (dev < kDevs) cache[dev] = n;
+  return n;
+}
+
 template <int NB>
 cudaError_t launch_nb(const GemmLnArgs& g, const DeviceCtl& ctl) {
-  using C = LnCfg<NB>;
+  // the pair form wherever the column chunks split into whole blocks
+  constexpr bool kPair = NB % 2 == 0;
+  using C = LnCfg<NB, kPair>;
   CUtensorMap ta, tw, tr;
   const uint64_t adims[2] = {static_cast<uint64_t>(g.K), static_cast<uint64_t>(g.M)};
   const uint64_t astr[1] = {static_cast<uint64_t>(g.K) * 2};
   const uint32_t abox[2] = {64, 128};
   // W [K, N] as a 3-D tensor (64 columns, K rows, NB column blocks): one
-  // copy per stage brings all NB blocks
+  // copy brings kPB blocks (all NB of them in the single-CTA form)
   const uint64_t wdims[3] = {64, static_cast<uint64_t>(g.K), static_cast<uint64_t>(NB)};
   const uint64_t wstr[2] = {static_cast<uint64_t>(C::N) * 2, 128};
-  const uint32_t wbox[3] = {64, 64, NB};
+  const uint32_t wbox[3] = {64, 64, static_cast<uint32_t>(C::kPB)};
   if (!encode_tensor_map(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(g.A), adims,
                          astr, abox, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_tensor_map(&tw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(g.W), wdims,
@@ -443,18 +606,39 @@ cudaError_t launch_nb(const GemmLnArgs& g, const DeviceCtl& ctl) {
   p.out_f32 = g.out_dtype == MHA_F32 ? 1 : 0;
   p.M = g.M;
   p.K = g.K;
-  p.mt = (g.M + kBM - 1) / kBM;
+  p.mt = (g.M + C::kTileM - 1) / C::kTileM;
   p.err = ctl.err;
   p.limit_ns = ctl.limit_ns;
-  auto kern = gemm_ln_bf16_kernel<NB>;
+  auto kern = gemm_ln_bf16_kernel<NB, kPair>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  // one CTA per SM at most (tensor memory and shared memory admit no second)
-  const int sms = current_sm_count();
-  const int grid = p.mt < sms ? p.mt : sms;
-  kern<<<grid, kThreads, C::kSmemBytes, g.stream>>>(ta, tw, tr, p);
-  return cudaGetLastError();
+  if constexpr (kPair) {
+    // one cluster of two per tile, as many as can be resident at once
+    const int slots = pair_slots<NB>();
+    const int pairs = p.mt < slots ? p.mt : slots;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cfg.stream = g.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, ta, tw, tr, p);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+  } else {
+    // one CTA per SM at most (tensor memory and shared memory admit no second)
+    const int sms = current_sm_count();
+    const int grid = p.mt < sms ? p.mt : sms;
+    kern<<<grid, kThreads, C::kSmemBytes, g.stream>>>(ta, tw, tr, p);
+    return cudaGetLastError();
+  }
 }
 
 }  // namespace
