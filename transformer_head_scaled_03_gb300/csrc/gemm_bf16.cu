@@ -30,6 +30,7 @@
 // while the next tile's MMAs run, and the TMA ring runs on across tiles.
 #include "internal.h"
 #include "ptx.cuh"
+#include "ptx_cluster.cuh"
 
 namespace mha {
 namespace {
@@ -54,8 +55,9 @@ constexpr int bDrain = 2 * kStages + 4;
 constexpr int kNumBars = 2 * kStages + 5;
 constexpr int kOffBar = kStages * kStageBytes;
 constexpr int kOffMisc = kOffBar + 8 * kNumBars;
-// epilogue staging: per epilogue warp, 32 rows x 128 bytes (64 bf16 columns)
-constexpr int kOffStage = (kOffMisc + 16 + 127) & ~127;
+// epilogue staging: per epilogue warp, 32 rows x 128 bytes (64 bf16 columns),
+// 1024-byte aligned: the layout is the TMA's 128-byte swizzle
+constexpr int kOffStage = (kOffMisc + 16 + 1023) & ~1023;
 constexpr int kStageWarpBytes = 32 * 128;
 constexpr int kSmemBytes = kOffStage + kEpiWarps * kStageWarpBytes + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory");
@@ -67,6 +69,7 @@ struct GemmParams {
   int store[3];
   int L[3];
   int dh[3];
+  int tstore[3];      // 1: the output leaves by TMA stores through tC*
   int M, N, K;
   int count;          // problems in the launch (1..3)
   int mt, nt;         // row and column tiles per problem
@@ -85,7 +88,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap tA0, const __grid_constant__ CUtensorMap tA1,
                      const __grid_constant__ CUtensorMap tA2, const __grid_constant__ CUtensorMap tW0,
                      const __grid_constant__ CUtensorMap tW1, const __grid_constant__ CUtensorMap tW2,
-                     const GemmParams p) {
+                     const __grid_constant__ CUtensorMap tC0, const __grid_constant__ CUtensorMap tC1,
+                     const __grid_constant__ CUtensorMap tC2, const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -98,6 +102,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const WaitCtl ctl{abort_flag, p.err, p.limit_ns};
   auto map_a = [&](int z) { return z == 0 ? &tA0 : (z == 1 ? &tA1 : &tA2); };
   auto map_w = [&](int z) { return z == 0 ? &tW0 : (z == 1 ? &tW1 : &tW2); };
+  auto map_c = [&](int z) { return z == 0 ? &tC0 : (z == 1 ? &tC1 : &tC2); };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -224,6 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // with m = bb * L + l and n = hh * dh + c.  Each lane computes the row
       // part of its own row (row `row` of the tile) once per tile.
       const bool split = store == static_cast<int>(GemmStore::kHeadSplit);
+      const bool tstore = p.tstore[z] != 0;
       long long row_part;
       if (split) {
         const int bb = m / L, l = m - bb * L;
@@ -270,8 +276,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(tbase + cb * 32, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
         tmem_ld32(tbase + cb * 32 + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
         tmem_ld_wait(v);
+        if (tstore) {
+          // the previous piece's TMA store has read the staging rows
+          if (lane == 0) bulk_wait_read0();
+          __syncwarp();
+        }
 #pragma unroll
         for (int q = 0; q < 8; ++q) stg[lane * 8 + (q ^ (lane & 7))] = finish8(&v[8 * q], n + 8 * q);
+        if (tstore) {
+          // the warp's 32 rows x 64 columns leave in one TMA store: 2-D
+          // (n, m) row-major, or 4-D (c, l, head, batch) for the head split
+          fence_proxy_async_smem();
+          __syncwarp();
+          const int mw = m0 + quarter * 32;
+          if (lane == 0 && mw < p.M) {
+            const uint32_t src = smem_u32(stg);
+            if (split) {
+              const int bb = mw / L, hh = n / dh;
+              tma_store_4d(map_c(z), src, n - hh * dh, mw - bb * L, hh, bb);
+            } else {
+              tma_store_2d(map_c(z), src, n, mw);
+            }
+            bulk_commit();
+          }
+          continue;
+        }
         __syncwarp();
         // four rows of 128 bytes per store instruction: lane l takes piece
         // l % 8 of row 4 g4 + l / 8
@@ -303,6 +332,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(bar(bAccEmpty(b)));
     }
+    // every TMA store of this warp has written global memory before the CTA ends
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -327,7 +359,7 @@ int num_sms() {
 cudaError_t launch_gemm_bf16(const GemmArgs& g, const DeviceCtl& ctl) {
   if (g.M == 0 || g.N == 0) return cudaSuccess;
   if (g.N % 64 != 0) return cudaErrorInvalidValue;  // W is copied in 64-column blocks
-  CUtensorMap ta[3], tw[3];
+  CUtensorMap ta[3], tw[3], tc[3];
   GemmParams p{};
   for (int i = 0; i < 3; ++i) {
     const GemmProblem& pr = g.prob[i < g.count ? i : 0];
@@ -343,6 +375,28 @@ cudaError_t launch_gemm_bf16(const GemmArgs& g, const DeviceCtl& ctl) {
         !encode_tensor_map(&tw[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(pr.W),
                            wdims, wstr, wbox, CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
+    // C by TMA stores of 32 rows x 64 columns: row-major [M, N], or the head
+    // split [B, H, L, dh] as 4-D (dh, L, H, B) when a 64-column piece lies in
+    // one head and a warp's 32 rows in one batch item; otherwise (or if the
+    // map cannot be made, e.g. an unaligned C) by the threads' own stores
+    p.tstore[i] = 0;
+    if (pr.store == GemmStore::kRowMajor) {
+      const uint64_t cdims[2] = {static_cast<uint64_t>(g.N), static_cast<uint64_t>(g.M)};
+      const uint64_t cstr[1] = {static_cast<uint64_t>(g.N) * 2};
+      const uint32_t cbox[2] = {64, 32};
+      p.tstore[i] = encode_tensor_map(&tc[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pr.C, cdims,
+                                      cstr, cbox, CU_TENSOR_MAP_SWIZZLE_128B) ? 1 : 0;
+    } else if (pr.dh > 0 && pr.dh % 64 == 0 && pr.L > 0 && pr.L % 32 == 0 && g.M % pr.L == 0 &&
+               g.N % pr.dh == 0) {
+      const uint64_t H = static_cast<uint64_t>(g.N / pr.dh), L = static_cast<uint64_t>(pr.L);
+      const uint64_t dh = static_cast<uint64_t>(pr.dh);
+      const uint64_t cdims[4] = {dh, L, H, static_cast<uint64_t>(g.M / pr.L)};
+      const uint64_t cstr[3] = {dh * 2, L * dh * 2, H * L * dh * 2};
+      const uint32_t cbox[4] = {64, 32, 1, 1};
+      p.tstore[i] = encode_tensor_map(&tc[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, pr.C, cdims,
+                                      cstr, cbox, CU_TENSOR_MAP_SWIZZLE_128B) ? 1 : 0;
+    }
+    if (!p.tstore[i]) tc[i] = tw[i];  // unused; any valid map fills the slot
     p.C[i] = pr.C;
     p.bias[i] = static_cast<const __nv_bfloat16*>(pr.bias);
     p.relu[i] = pr.relu;
@@ -366,7 +420,7 @@ cudaError_t launch_gemm_bf16(const GemmArgs& g, const DeviceCtl& ctl) {
   const long long tiles = static_cast<long long>(p.mt) * p.nt * g.count;
   const int grid = static_cast<int>(tiles < num_sms() ? tiles : num_sms());
   gemm_bf16_kernel<<<grid, kThreads, kSmemBytes, g.stream>>>(ta[0], ta[1], ta[2], tw[0], tw[1],
-                                                              tw[2], p);
+                                                              tw[2], tc[0], tc[1], tc[2], p);
   return cudaGetLastError();
 }
 
