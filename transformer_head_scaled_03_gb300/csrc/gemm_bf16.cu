@@ -31,6 +31,7 @@
 #include "internal.h"
 #include "ptx.cuh"
 #include "ptx_cluster.cuh"
+#include "ptx_store.cuh"
 
 namespace mha {
 namespace {
