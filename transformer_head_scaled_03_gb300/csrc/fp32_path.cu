@@ -441,28 +441,29 @@ __global__ void __launch_bounds__(256) gemm_f32_kernel(const GemmF32Params p) {
   }
 }
 
-// Small-M form: BM x 32 CTA tiles with the k-step split four ways inside the
-// CTA.  The 256 threads are four groups of 64; group g multiplies k-columns
-// 8g..8g+7 of every staged k-step, each thread a (BM / 8) x 4 block of the
-// tile (rows ty, ty+8, ...: conflict-free A reads).  The four partial
-// tiles are summed through shared memory at the end, in a fixed order.  It
-// puts four times as many warps on each output tile as the plain form, for
-// problems too small to fill the GPU with CTAs (a 128-row layer).
-template <bool kVec, int BM>
+// Small-M form: 16 x 32 CTA tiles with the k-step split eight ways inside the
+// CTA.  Warp g multiplies k-columns 4g..4g+3 of every staged k-step, each
+// lane a 4 x 4 block of the tile (rows ty + 4i, columns 4tx..4tx+3): one
+// 16-byte load brings a row's four k values of A, one a k row's four columns
+// of W, so 8 shared-memory loads feed 64 FMAs (both conflict-free).  The
+// eight partial tiles are summed through shared memory at the end, in a fixed
+// order.  It puts eight warps on each output tile, for problems too small to
+// fill the GPU with CTAs (a 128-row layer).
+template <bool kVec, int BM, int NS>
 __global__ void __launch_bounds__(256) gemm_f32_splitk_kernel(const GemmF32Params p) {
   constexpr int BN = 32;
-  constexpr int RM = BM / 8;  // rows per thread
+  static_assert(BM == 16, "a warp covers 16 rows x 32 columns in 4 x 4 blocks");
   extern __shared__ __align__(16) float gsm[];
   float (*As)[BM][kApad] = reinterpret_cast<float (*)[BM][kApad]>(gsm);
-  float (*Ws)[kBK][BN] = reinterpret_cast<float (*)[kBK][BN]>(gsm + kStages * BM * kApad);
+  float (*Ws)[kBK][BN] = reinterpret_cast<float (*)[kBK][BN]>(gsm + NS * BM * kApad);
   const int z = blockIdx.z;
   const float* __restrict__ A = p.A[z];
   const float* __restrict__ W = p.W[z];
   const int M = p.M, N = p.N, K = p.K;
   const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
   const int tid = threadIdx.x;
-  const int grp = tid >> 6, t = tid & 63;
-  const int ty = t >> 3, tx = t & 7;  // rows ty + 8i, columns 4tx..4tx+3
+  const int grp = tid >> 5, lane = tid & 31;
+  const int ty = lane >> 3, tx = lane & 7;  // rows ty + 4i, columns 4tx..4tx+3
   const int num_k = (K + kBK - 1) / kBK;
 
   auto load_tile = [&](int kt, int buf) {
@@ -497,27 +498,30 @@ __global__ void __launch_bounds__(256) gemm_f32_splitk_kernel(const GemmF32Param
     }
   };
 
-  float acc[RM][4] = {};
+  float acc[4][4] = {};
 #pragma unroll
-  for (int st = 0; st < kStages - 1; ++st) {
+  for (int st = 0; st < NS - 1; ++st) {
     if (st < num_k) load_tile(st, st);
     if constexpr (kVec) cp_async_commit();
   }
   for (int kt = 0; kt < num_k; ++kt) {
-    const int buf = kt % kStages;
-    if constexpr (kVec) cp_async_wait<kStages - 2>();
+    const int buf = kt % NS;
+    if constexpr (kVec) cp_async_wait<NS - 2>();
     __syncthreads();
     {
-      const int kn = kt + kStages - 1;
-      if (kn < num_k) load_tile(kn, kn % kStages);
+      const int kn = kt + NS - 1;
+      if (kn < num_k) load_tile(kn, kn % NS);
       if constexpr (kVec) cp_async_commit();
     }
+    float4 a4[4];
 #pragma unroll
-    for (int kk = grp * 8; kk < grp * 8 + 8; ++kk) {
-      const float4 w = *reinterpret_cast<const float4*>(&Ws[buf][kk][4 * tx]);
+    for (int i = 0; i < 4; ++i) a4[i] = *reinterpret_cast<const float4*>(&As[buf][ty + 4 * i][4 * grp]);
 #pragma unroll
-      for (int i = 0; i < RM; ++i) {
-        const float a = As[buf][ty + 8 * i][kk];
+    for (int kk = 0; kk < 4; ++kk) {
+      const float4 w = *reinterpret_cast<const float4*>(&Ws[buf][4 * grp + kk][4 * tx]);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float a = kk == 0 ? a4[i].x : kk == 1 ? a4[i].y : kk == 2 ? a4[i].z : a4[i].w;
         acc[i][0] = fmaf(a, w.x, acc[i][0]);
         acc[i][1] = fmaf(a, w.y, acc[i][1]);
         acc[i][2] = fmaf(a, w.z, acc[i][2]);
@@ -526,12 +530,12 @@ __global__ void __launch_bounds__(256) gemm_f32_splitk_kernel(const GemmF32Param
     }
   }
   if constexpr (kVec) cp_async_wait<0>();
-  __syncthreads();  // the stages are free: reuse them for the four partial tiles
+  __syncthreads();  // the stages are free: reuse them for the eight partial tiles
   float (*red)[BM][BN + 1] = reinterpret_cast<float (*)[BM][BN + 1]>(gsm);
 #pragma unroll
-  for (int i = 0; i < RM; ++i)
+  for (int i = 0; i < 4; ++i)
 #pragma unroll
-    for (int j = 0; j < 4; ++j) red[grp][ty + 8 * i][4 * tx + j] = acc[i][j];
+    for (int j = 0; j < 4; ++j) red[grp][ty + 4 * i][4 * tx + j] = acc[i][j];
   __syncthreads();
   float* C = p.C[z];
   const bool split = p.store[z] == static_cast<int>(GemmStore::kHeadSplit);
@@ -543,7 +547,8 @@ __global__ void __launch_bounds__(256) gemm_f32_splitk_kernel(const GemmF32Param
     const int r = o >> 5, c = o & 31;
     const int m = m0 + r, n = n0 + c;
     if (m >= M || n >= N) continue;
-    float v = (red[0][r][c] + red[1][r][c]) + (red[2][r][c] + red[3][r][c]);
+    float v = ((red[0][r][c] + red[1][r][c]) + (red[2][r][c] + red[3][r][c])) +
+              ((red[4][r][c] + red[5][r][c]) + (red[6][r][c] + red[7][r][c]));
     size_t off;
     if (split) {
       const int L = p.L[z], dh = p.dh[z];
@@ -558,17 +563,29 @@ __global__ void __launch_bounds__(256) gemm_f32_splitk_kernel(const GemmF32Param
   }
 }
 
-template <bool kVec>
-cudaError_t launch_gemm_f32_splitk(const GemmF32Params& p, int count, cudaStream_t s) {
+template <bool kVec, int NS>
+cudaError_t launch_splitk_ns(const GemmF32Params& p, int count, cudaStream_t s) {
   constexpr int BM = kSplitBM;
   const dim3 grid((p.N + 31) / 32, (p.M + BM - 1) / BM, count);
-  auto kern = gemm_f32_splitk_kernel<kVec, BM>;
-  constexpr int smem = kStages * (BM * kApad + kBK * 32) * 4;
-  static_assert(smem >= 4 * BM * 33 * 4, "partial tiles fit in the stages");
+  auto kern = gemm_f32_splitk_kernel<kVec, BM, NS>;
+  constexpr int smem = NS * (BM * kApad + kBK * 32) * 4;
+  static_assert(smem >= 8 * BM * 33 * 4, "partial tiles fit in the stages");
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   kern<<<grid, 256, smem, s>>>(p);
   return cudaGetLastError();
+}
+
+// The ring is as deep as residency allows: a 128-row layer's GEMM is a chain
+// of k-steps waiting on L2, so more k-steps in flight shorten it, as long as
+// the grid still fits on the GPU at once (a stage is 6.4 KB: 16 stages keep two
+// CTAs per SM, 8 keep four).
+template <bool kVec>
+cudaError_t launch_gemm_f32_splitk(const GemmF32Params& p, int count, cudaStream_t s, int sms) {
+  const long long ctas = static_cast<long long>((p.N + 31) / 32) * ((p.M + kSplitBM - 1) / kSplitBM) * count;
+  if (ctas <= 2LL * sms) return launch_splitk_ns<kVec, 16>(p, count, s);
+  if (ctas <= 4LL * sms) return launch_splitk_ns<kVec, 8>(p, count, s);
+  return launch_splitk_ns<kVec, 4>(p, count, s);
 }
 
 template <bool kVec, int BN>
@@ -656,8 +673,8 @@ cudaError_t launch_gemm_f32(const GemmArgs& g, const DeviceCtl&) {
     return cudaErrorInvalidValue;
   const long long wide = static_cast<long long>((g.N + 63) / 64) * ((g.M + kBM - 1) / kBM) * g.count;
   if (wide < sms)
-    return vec ? launch_gemm_f32_splitk<true>(p, g.count, g.stream)
-               : launch_gemm_f32_splitk<false>(p, g.count, g.stream);
+    return vec ? launch_gemm_f32_splitk<true>(p, g.count, g.stream, sms)
+               : launch_gemm_f32_splitk<false>(p, g.count, g.stream, sms);
   return vec ? launch_gemm_f32_tiles<true, 64>(p, g.count, g.stream)
              : launch_gemm_f32_tiles<false, 64>(p, g.count, g.stream);
 }
