@@ -145,15 +145,24 @@ __global__ void __launch_bounds__(kWarps * 32) sdpa_f32_kernel(const SdpaF32Para
     }
   };
   const int n_chunks = (kv_stop + kKeys - 1) / kKeys;
+  // the Q rows are requested first, so that their loads are not queued behind
+  // the two chunks' copies; they are scaled and stored once those are issued
+  constexpr int kQPerThread = kRowsC * DP / (kWarps * 32);
+  static_assert(kQPerThread * kWarps * 32 == kRowsC * DP, "Q tile split over the threads");
+  float qv[kQPerThread];
+#pragma unroll
+  for (int i = 0; i < kQPerThread; ++i) {
+    const int idx = threadIdx.x + kWarps * 32 * i;
+    const int r = idx / DP, c = idx % DP;
+    const int q = row0 + r;
+    qv[i] = (q < p.Lq && c < d) ? __ldg(p.Q + (bh * p.Lq + q) * d + c) : 0.f;
+  }
   if (n_chunks > 0) load_chunk(0);
   cp_async_commit();
   if (n_chunks > 1) load_chunk(1);
   cp_async_commit();
-  for (int idx = threadIdx.x; idx < kRowsC * DP; idx += blockDim.x) {
-    const int r = idx / DP, c = idx % DP;
-    const int q = row0 + r;
-    sQ[idx] = (q < p.Lq && c < d) ? p.Q[(bh * p.Lq + q) * d + c] * p.scale : 0.f;
-  }
+#pragma unroll
+  for (int i = 0; i < kQPerThread; ++i) sQ[threadIdx.x + kWarps * 32 * i] = qv[i] * p.scale;
   const int grp = warp / kGroupWarps, wg = warp % kGroupWarps;
   // this lane's keys within a chunk: 32 (grp KPL + t) + lane, t < KPL
   auto key_of = [&](int t) { return 32 * (grp * KPL + t) + lane; };
