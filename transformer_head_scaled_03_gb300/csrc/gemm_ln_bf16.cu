@@ -13,8 +13,18 @@
 //
 // A CTA's output tile is 128 rows x N columns with N = d_model <= 512, i.e.
 // whole rows: the fp32 accumulator holds N of the 512 tensor-memory columns
-// and each epilogue thread owns one row.  The epilogue makes two passes
-// over the row in tensor memory:
+// and each epilogue thread owns one row, half of its columns.
+//
+// When N is an even number of 64-column blocks, two CTAs on two SMs (a
+// cluster) share a tile of 256 rows: the even CTA issues M = 256 products
+// (tcgen05 .cta_group::2) whose A rows and W columns are split between the
+// two CTAs' shared memory, so each SM stages 128 rows of A and half of W per
+// k-step (48 KB at N = 512 instead of 80 KB, three stages instead of two),
+// and each CTA's tensor memory receives its own 128 rows.  Odd block counts
+// run the same code as one CTA per tile.
+//
+// The epilogue makes two passes over the row in tensor memory, two warps per
+// lane quarter, each taking half of the row's 64-column chunks:
 //   1. v = acc + bias + R (R arrives by TMA, 32 rows x 64 columns per warp
 //      and chunk, in a two-buffer ring whose first chunks load while the
 //      MMAs run; bias, gamma and beta sit in shared memory); per
@@ -22,17 +32,19 @@
 //      chunk by chunk with the pairwise update of Chan, Golub and LeVeque
 //      ("Updating formulae and a pairwise algorithm for computing sample
 //      variances", 1979): no E[v^2] - E[v]^2 cancellation; v goes back into
-//      tensor memory;
+//      tensor memory.  The two warps of a quarter then swap their halves'
+//      (mean, M2) through shared memory and merge them the same way, in the
+//      same order, so both normalise with identical values;
 //   2. y = (v - mean) / sqrt(var + eps) * gamma + beta, population variance
 //      (divisor N), stored as bf16 or fp32 through a per-warp shared-memory
 //      transpose, so that each store instruction writes four whole 128-byte
 //      row pieces.
-// Row tile t walks its k-steps starting at t mod (K / 64): all CTAs share
-// W, and staggering keeps them from asking the same L2 lines at once.
-// Warp roles and the TMA ring are those of the plain projection kernel:
-// warp 0 TMA producer, warp 1 MMA issuer and TMEM owner, warps 2-5 epilogue.
-// One accumulator: the next tile's MMAs wait for the epilogue, while the TMA
-// ring keeps loading ahead.
+// Tile t walks its k-steps starting at t mod (K / 64): all CTAs share W, and
+// staggering keeps them from asking the same L2 lines at once.
+// Warp roles: warp 0 TMA producer, warp 1 MMA issuer and TMEM owner (the
+// even CTA's issues for the pair), warps 2-9 epilogue.  One accumulator: the
+// next tile's MMAs wait for the epilogue (of both CTAs), while the TMA ring
+// keeps loading ahead.
 #include "internal.h"
 #include "ptx.cuh"
 #include "ptx_cluster.cuh"
