@@ -260,6 +260,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+      // Every copy lands before the CTA exits.  In the pair form all of
+      // them (the other CTA's too) report to rank 0's full barriers, so rank
+      // 0 waits on those; the other CTA leaves only after the final cluster
+      // barrier, which rank 0 reaches after this wait.
       if (rank == 0)
         for (int q = max(0, g - C::kStages); q < g; ++q)
           wait_drain(bar(C::bFull(q % C::kStages)), (q / C::kStages) & 1, p.limit_ns);
