@@ -122,3 +122,27 @@ def test_encoder_rejects_unsupported_shapes():
             layer.forward(torch.zeros((1, 17, D), device="cuda"), p)
     finally:
         layer.close()
+
+
+def test_encoder_layer_is_deterministic():
+    """The layer's sums have fixed orders (no atomics; the two epilogue warps
+    of a row merge their statistics in one order; CTA pairs split rows and
+    columns, never a sum across CTAs), so repeated calls give the same bits.
+    20,480 rows at d_model 256: more CTA-pair tiles than pairs resident."""
+    B, L, D, h, F = 64, 320, 256, 4, 1024
+    st = "bf16"
+    g = Draws(77)
+    p = {k: torch.from_numpy(v).to(torch.bfloat16).cuda()
+         for k, v in make_params(g, D, F, st).items()}
+    x = torch.from_numpy(g.normal((B, L, D), dtype=st)).to(torch.bfloat16).cuda()
+    lens = torch.from_numpy(g.integers(L // 2, L, B)).cuda()
+    layer = mha.EncoderLayer(D, h, F, torch.bfloat16, B, L)
+    try:
+        outs = [layer.forward(x, p, mask_kind=mha.MASK_KEY_PADDING, key_lengths=lens,
+                              out_dtype=torch.float32).clone() for _ in range(4)]
+        assert mha.mha_check() == mha.MHA_OK
+    finally:
+        layer.close()
+    assert bool(torch.isfinite(outs[0]).all())
+    for o in outs[1:]:
+        assert torch.equal(o, outs[0])
