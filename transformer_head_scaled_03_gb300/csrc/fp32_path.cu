@@ -458,16 +458,17 @@ __global__ void __launch_bounds__(256) gemm_f32_kernel(const GemmF32Params p) {
 // eight partial tiles are summed through shared memory at the end, in a fixed
 // order.  It puts eight warps on each output tile, for problems too small to
 // fill the GPU with CTAs (a 128-row layer).
-template <bool kVec, int BM, int NS>
+template <bool kVec, int BM, int NS, int CNT>
 __global__ void __launch_bounds__(256) gemm_f32_splitk_kernel(const GemmF32Params p) {
+  // CNT problems per CTA (1, or 3 when the three share A: the same tile of
+  // Q, K and V from one staged tile of x)
   constexpr int BN = 32;
   static_assert(BM == 16, "a warp covers 16 rows x 32 columns in 4 x 4 blocks");
   extern __shared__ __align__(16) float gsm[];
   float (*As)[BM][kApad] = reinterpret_cast<float (*)[BM][kApad]>(gsm);
-  float (*Ws)[kBK][BN] = reinterpret_cast<float (*)[kBK][BN]>(gsm + NS * BM * kApad);
-  const int z = blockIdx.z;
-  const float* __restrict__ A = p.A[z];
-  const float* __restrict__ W = p.W[z];
+  float (*Ws)[CNT][kBK][BN] = reinterpret_cast<float (*)[CNT][kBK][BN]>(gsm + NS * BM * kApad);
+  const int z0 = blockIdx.z * CNT;
+  const float* __restrict__ A = p.A[z0];
   const int M = p.M, N = p.N, K = p.K;
   const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
   const int tid = threadIdx.x;
@@ -485,11 +486,13 @@ __global__ void __launch_bounds__(256) gemm_f32_splitk_kernel(const GemmF32Param
         cp_async16(static_cast<uint32_t>(__cvta_generic_to_shared(&As[buf][r][c4])),
                    in ? A + static_cast<size_t>(gm) * K + gk : A, in ? 16u : 0u);
       }
-      {  // W: 32 rows x 8 chunks
+#pragma unroll
+      for (int zz = 0; zz < CNT; ++zz) {  // W: 32 rows x 8 chunks per problem
+        const float* __restrict__ W = p.W[z0 + zz];
         const int r = tid >> 3, c4 = (tid & 7) * 4;
         const int gk = k0 + r, gn = n0 + c4;
         const bool in = gk < K && gn < N;
-        cp_async16(static_cast<uint32_t>(__cvta_generic_to_shared(&Ws[buf][r][c4])),
+        cp_async16(static_cast<uint32_t>(__cvta_generic_to_shared(&Ws[buf][zz][r][c4])),
                    in ? W + static_cast<size_t>(gk) * N + gn : W, in ? 16u : 0u);
       }
     } else {
@@ -502,12 +505,15 @@ __global__ void __launch_bounds__(256) gemm_f32_splitk_kernel(const GemmF32Param
           As[buf][r][c] = (gm < M && gk < K) ? A[static_cast<size_t>(gm) * K + gk] : 0.f;
         }
         const int gk2 = k0 + r, gn = n0 + c;
-        Ws[buf][r][c] = (gk2 < K && gn < N) ? W[static_cast<size_t>(gk2) * N + gn] : 0.f;
+#pragma unroll
+        for (int zz = 0; zz < CNT; ++zz)
+          Ws[buf][zz][r][c] =
+              (gk2 < K && gn < N) ? p.W[z0 + zz][static_cast<size_t>(gk2) * N + gn] : 0.f;
       }
     }
   };
 
-  float acc[4][4] = {};
+  float acc[CNT][4][4] = {};
 #pragma unroll
   for (int st = 0; st < NS - 1; ++st) {
     if (st < num_k) load_tile(st, st);
@@ -527,58 +533,68 @@ __global__ void __launch_bounds__(256) gemm_f32_splitk_kernel(const GemmF32Param
     for (int i = 0; i < 4; ++i) a4[i] = *reinterpret_cast<const float4*>(&As[buf][ty + 4 * i][4 * grp]);
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {
-      const float4 w = *reinterpret_cast<const float4*>(&Ws[buf][4 * grp + kk][4 * tx]);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float a = kk == 0 ? a4[i].x : kk == 1 ? a4[i].y : kk == 2 ? a4[i].z : a4[i].w;
-        acc[i][0] = fmaf(a, w.x, acc[i][0]);
-        acc[i][1] = fmaf(a, w.y, acc[i][1]);
-        acc[i][2] = fmaf(a, w.z, acc[i][2]);
-        acc[i][3] = fmaf(a, w.w, acc[i][3]);
+      for (int zz = 0; zz < CNT; ++zz) {
+        const float4 w = *reinterpret_cast<const float4*>(&Ws[buf][zz][4 * grp + kk][4 * tx]);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float a = kk == 0 ? a4[i].x : kk == 1 ? a4[i].y : kk == 2 ? a4[i].z : a4[i].w;
+          acc[zz][i][0] = fmaf(a, w.x, acc[zz][i][0]);
+          acc[zz][i][1] = fmaf(a, w.y, acc[zz][i][1]);
+          acc[zz][i][2] = fmaf(a, w.z, acc[zz][i][2]);
+          acc[zz][i][3] = fmaf(a, w.w, acc[zz][i][3]);
+        }
       }
     }
   }
   if constexpr (kVec) cp_async_wait<0>();
   __syncthreads();  // the stages are free: reuse them for the eight partial tiles
-  float (*red)[BM][BN + 1] = reinterpret_cast<float (*)[BM][BN + 1]>(gsm);
+  float (*red)[8][BM][BN + 1] = reinterpret_cast<float (*)[8][BM][BN + 1]>(gsm);
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
+  for (int zz = 0; zz < CNT; ++zz)
 #pragma unroll
-    for (int j = 0; j < 4; ++j) red[grp][ty + 4 * i][4 * tx + j] = acc[i][j];
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) red[zz][grp][ty + 4 * i][4 * tx + j] = acc[zz][i][j];
   __syncthreads();
-  float* C = p.C[z];
-  const bool split = p.store[z] == static_cast<int>(GemmStore::kHeadSplit);
-  const float* bias = p.bias[z];
-  const bool relu = p.relu[z] != 0;
 #pragma unroll
-  for (int e = 0; e < BM / 8; ++e) {
-    const int o = tid + 256 * e;
-    const int r = o >> 5, c = o & 31;
-    const int m = m0 + r, n = n0 + c;
-    if (m >= M || n >= N) continue;
-    float v = ((red[0][r][c] + red[1][r][c]) + (red[2][r][c] + red[3][r][c])) +
-              ((red[4][r][c] + red[5][r][c]) + (red[6][r][c] + red[7][r][c]));
-    size_t off;
-    if (split) {
-      const int L = p.L[z], dh = p.dh[z];
-      const int bb = m / L, l = m - bb * L, hh = n / dh, cc = n - hh * dh;
-      off = ((static_cast<size_t>(bb) * (N / dh) + hh) * L + l) * dh + cc;
-    } else {
-      off = static_cast<size_t>(m) * N + n;
+  for (int zz = 0; zz < CNT; ++zz) {
+    const int z = z0 + zz;
+    float* C = p.C[z];
+    const bool split = p.store[z] == static_cast<int>(GemmStore::kHeadSplit);
+    const float* bias = p.bias[z];
+    const bool relu = p.relu[z] != 0;
+#pragma unroll
+    for (int e = 0; e < BM / 8; ++e) {
+      const int o = tid + 256 * e;
+      const int r = o >> 5, c = o & 31;
+      const int m = m0 + r, n = n0 + c;
+      if (m >= M || n >= N) continue;
+      float v = ((red[zz][0][r][c] + red[zz][1][r][c]) + (red[zz][2][r][c] + red[zz][3][r][c])) +
+                ((red[zz][4][r][c] + red[zz][5][r][c]) + (red[zz][6][r][c] + red[zz][7][r][c]));
+      size_t off;
+      if (split) {
+        const int L = p.L[z], dh = p.dh[z];
+        const int bb = m / L, l = m - bb * L, hh = n / dh, cc = n - hh * dh;
+        off = ((static_cast<size_t>(bb) * (N / dh) + hh) * L + l) * dh + cc;
+      } else {
+        off = static_cast<size_t>(m) * N + n;
+      }
+      if (bias) v += bias[n];
+      if (relu) v = fmaxf(v, 0.f);
+      C[off] = v;
     }
-    if (bias) v += bias[n];
-    if (relu) v = fmaxf(v, 0.f);
-    C[off] = v;
   }
 }
 
-template <bool kVec, int NS>
+template <bool kVec, int NS, int CNT>
 cudaError_t launch_splitk_ns(const GemmF32Params& p, int count, cudaStream_t s) {
   constexpr int BM = kSplitBM;
-  const dim3 grid((p.N + 31) / 32, (p.M + BM - 1) / BM, count);
-  auto kern = gemm_f32_splitk_kernel<kVec, BM, NS>;
-  constexpr int smem = NS * (BM * kApad + kBK * 32) * 4;
-  static_assert(smem >= 8 * BM * 33 * 4, "partial tiles fit in the stages");
+  const dim3 grid((p.N + 31) / 32, (p.M + BM - 1) / BM, count / CNT);
+  auto kern = gemm_f32_splitk_kernel<kVec, BM, NS, CNT>;
+  constexpr int smem = NS * (BM * kApad + CNT * kBK * 32) * 4;
+  static_assert(smem >= CNT * 8 * BM * 33 * 4, "partial tiles fit in the stages");
+  static_assert(smem <= 232448, "shared memory");
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   kern<<<grid, 256, smem, s>>>(p);
@@ -588,13 +604,19 @@ cudaError_t launch_splitk_ns(const GemmF32Params& p, int count, cudaStream_t s) 
 // The ring is as deep as residency allows: a 128-row layer's GEMM is a chain
 // of k-steps waiting on L2, so more k-steps in flight shorten it, as long as
 // the grid still fits on the GPU at once (a stage is 6.4 KB: 16 stages keep two
-// CTAs per SM, 8 keep four).
+// CTAs per SM, 8 keep four).  Three problems that share A (the Q, K and V
+// projections of self-attention) run as one CTA per tile position when that
+// fits on the GPU in one CTA per SM: x's tile is staged once for all three,
+// and each warp keeps three independent accumulator sets.
 template <bool kVec>
 cudaError_t launch_gemm_f32_splitk(const GemmF32Params& p, int count, cudaStream_t s, int sms) {
-  const long long ctas = static_cast<long long>((p.N + 31) / 32) * ((p.M + kSplitBM - 1) / kSplitBM) * count;
-  if (ctas <= 2LL * sms) return launch_splitk_ns<kVec, 16>(p, count, s);
-  if (ctas <= 4LL * sms) return launch_splitk_ns<kVec, 8>(p, count, s);
-  return launch_splitk_ns<kVec, 4>(p, count, s);
+  const long long pos = static_cast<long long>((p.N + 31) / 32) * ((p.M + kSplitBM - 1) / kSplitBM);
+  if (count == 3 && p.A[0] == p.A[1] && p.A[0] == p.A[2] && pos <= sms)
+    return launch_splitk_ns<kVec, 12, 3>(p, count, s);
+  const long long ctas = pos * count;
+  if (ctas <= 2LL * sms) return launch_splitk_ns<kVec, 16, 1>(p, count, s);
+  if (ctas <= 4LL * sms) return launch_splitk_ns<kVec, 8, 1>(p, count, s);
+  return launch_splitk_ns<kVec, 4, 1>(p, count, s);
 }
 
 template <bool kVec, int BN>
