@@ -665,8 +665,10 @@ def bench_mha_layer(w_shape, dtype_name, steps, warmup, local_rank, seed_w=None)
     try:
         # eager, and the same call captured once in a CUDA graph and replayed:
         # the library's device time without the per-call host overhead
-        eager_ms, graph_ms = _time_eager_and_graph(
-            lambda: mha.mha_forward(handle, x, x, *Ws, h=h, out=out), steps, warmup)
+        call = lambda: mha.mha_forward(handle, x, x, *Ws, h=h, out=out)
+        eager_ms, graph_ms = _time_eager_and_graph(call, steps, warmup)
+        layers_ms = (_time_graph_layers(call, GRAPH_LAYERS, max(steps, 60), warmup)
+                     if graph_ms < 1.0 else None)
         st = mha.mha_check(handle)
         if st != mha.MHA_OK:
             raise RuntimeError(mha.status_string(st))
@@ -682,6 +684,10 @@ def bench_mha_layer(w_shape, dtype_name, steps, warmup, local_rank, seed_w=None)
             "timing": "CUDA graph replay of one mha_forward call",
             "eager_tokens_per_s": round(B * L / (eager_ms / 1e3), 1),
             "eager_ms_per_layer": round(eager_ms, 4),
+            **({} if layers_ms is None else {
+                "graph6_tokens_per_s": round(B * L / (layers_ms / 1e3), 1),
+                "graph6_ms_per_layer": round(layers_ms, 4),
+                "graph6_timing": f"one CUDA graph of {GRAPH_LAYERS} back-to-back calls, per call"}),
             "gpu_launches_per_layer": 3}
 
 
@@ -723,8 +729,10 @@ def bench_encoder_layer(shape, dtype_name, steps, warmup, local_rank, key_paddin
     out = torch.empty_like(x)
     layer = mha.EncoderLayer(D, h, F, dtype, B, L)
     try:
-        eager_ms, graph_ms = _time_eager_and_graph(
-            lambda: layer.forward(x, p, mask_kind=mask, key_lengths=lens, out=out), steps, warmup)
+        call = lambda: layer.forward(x, p, mask_kind=mask, key_lengths=lens, out=out)
+        eager_ms, graph_ms = _time_eager_and_graph(call, steps, warmup)
+        layers_ms = (_time_graph_layers(call, GRAPH_LAYERS, max(steps, 60), warmup)
+                     if graph_ms < 1.0 else None)
         st = mha.mha_check()
         if st != mha.MHA_OK:
             raise RuntimeError(mha.status_string(st))
@@ -742,6 +750,10 @@ def bench_encoder_layer(shape, dtype_name, steps, warmup, local_rank, key_paddin
             "timing": "CUDA graph replay of one encoder_forward call",
             "eager_tokens_per_s": round(B * L / (eager_ms / 1e3), 1),
             "eager_ms_per_layer": round(eager_ms, 4),
+            **({} if layers_ms is None else {
+                "graph6_tokens_per_s": round(B * L / (layers_ms / 1e3), 1),
+                "graph6_ms_per_layer": round(layers_ms, 4),
+                "graph6_timing": f"one CUDA graph of {GRAPH_LAYERS} back-to-back calls, per call"}),
             "gpu_launches_per_layer": encoder_launches(dtype_name, D)}
 
 
@@ -1068,6 +1080,37 @@ def bench_backward(w, steps, warmup, local_rank, peak):
             "ms_per_call": round(ms, 4), "flops_per_call": flops, "tflops": round(tf, 2),
             "frac_of_peak": round(tf / peak, 4), "peak": peak, "grad_dtype": "bf16 dK dV, fp32 dQ",
             "gpu_launches_per_call": 2, "timing": "eager, CUDA events, inputs > L2"}
+
+
+GRAPH_LAYERS = 6  # calls captured in one graph for the per-layer device time (the base model's depth)
+
+
+def _time_graph_layers(step, n, steps, warmup):
+    """ms per call of ``step`` inside one CUDA graph of ``n`` back-to-back
+    calls: a single-call graph's replay also pays the graph launch, which for
+    a layer of a few tens of microseconds is a visible share of it."""
+    import torch
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for _ in range(n):
+            step()
+    for _ in range(warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    reps = max(1, steps // n)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        graph.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / (reps * n)
 
 
 def _time_eager_and_graph(step, steps, warmup):
