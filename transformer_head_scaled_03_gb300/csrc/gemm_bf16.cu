@@ -31,6 +31,7 @@
 #include "internal.h"
 #include "ptx.cuh"
 #include "ptx_cluster.cuh"
+#include "ptx_pdl.cuh"
 #include "ptx_store.cuh"
 
 namespace mha {
@@ -132,6 +133,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+  // the launch that follows may set itself up from here on; every access to
+  // data an earlier launch produced (A, the residual, C) comes after it ends
+  pdl_launch_dependents();
+  pdl_wait();
 
   const int num_k = (p.K + kBK - 1) / kBK;
   const int num_tiles = p.mt * p.count * p.nt;
@@ -420,8 +425,19 @@ cudaError_t launch_gemm_bf16(const GemmArgs& g, const DeviceCtl& ctl) {
   // when there are fewer tiles
   const long long tiles = static_cast<long long>(p.mt) * p.nt * g.count;
   const int grid = static_cast<int>(tiles < num_sms() ? tiles : num_sms());
-  gemm_bf16_kernel<<<grid, kThreads, kSmemBytes, g.stream>>>(ta[0], ta[1], ta[2], tw[0], tw[1],
-                                                              tw[2], tc[0], tc[1], tc[2], p);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = g.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, gemm_bf16_kernel, ta[0], ta[1], ta[2], tw[0], tw[1], tw[2], tc[0],
+                         tc[1], tc[2], p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

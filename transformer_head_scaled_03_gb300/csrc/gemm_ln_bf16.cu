@@ -48,6 +48,7 @@
 #include "internal.h"
 #include "ptx.cuh"
 #include "ptx_cluster.cuh"
+#include "ptx_pdl.cuh"
 #include "ptx_pair.cuh"
 
 namespace mha {
@@ -220,6 +221,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+  // the launch that follows may set itself up from here on; every access to
+  // data an earlier launch produced (A, the residual, C) comes after it ends
+  pdl_launch_dependents();
+  pdl_wait();
   const int num_k = (p.K + kBK - 1) / kBK;
 
   if (warp == 0) {
@@ -638,13 +643,15 @@ cudaError_t launch_nb(const GemmLnArgs& g, const DeviceCtl& ctl) {
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = C::kSmemBytes;
     cfg.stream = g.stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     e = cudaLaunchKernelEx(&cfg, kern, ta, tw, tr, p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
@@ -652,7 +659,18 @@ cudaError_t launch_nb(const GemmLnArgs& g, const DeviceCtl& ctl) {
     // one CTA per SM at most (tensor memory and shared memory admit no second)
     const int sms = current_sm_count();
     const int grid = p.mt < sms ? p.mt : sms;
-    kern<<<grid, kThreads, C::kSmemBytes, g.stream>>>(ta, tw, tr, p);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cfg.stream = g.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, ta, tw, tr, p);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
   }
 }
