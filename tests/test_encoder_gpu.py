@@ -62,6 +62,11 @@ CASES = [
     # the second with more 128-row tiles than SMs
     (torch.bfloat16, 2, 150, 320, 5, 640, mha.MASK_CAUSAL, None),
     (torch.bfloat16, 64, 320, 192, 3, 384, mha.MASK_NONE, None),
+    # d_model 128: the CTA-pair form with one 128-column chunk (one block of
+    # W per CTA); d_model 64: the single-CTA form, where the second epilogue
+    # warp of each lane quarter has no chunk of its own
+    (torch.bfloat16, 4, 96, 128, 2, 256, mha.MASK_CAUSAL, None),
+    (torch.bfloat16, 2, 100, 64, 1, 128, mha.MASK_KEY_PADDING, [100, 37]),
     (torch.float32, 1, 128, 512, 8, 2048, mha.MASK_NONE, None),
     (torch.float32, 2, 50, 96, 3, 200, mha.MASK_CAUSAL, None),
 ]
