@@ -17,9 +17,12 @@
 // thread about 100 cycles; five per stage would take as long as the stage's
 // MMAs.)  Warp roles: warp 0 TMA producer, warp 1 MMA issuer and TMEM
 // owner, warps 2-9 epilogue, two per TMEM lane quarter, each half of the
-// columns (TMEM -> registers, one row per thread; then through a
-// shared-memory transpose so that every store instruction writes whole
-// 128-byte row segments).
+// columns (TMEM -> registers, one row per thread; then a 32-row x 64-column
+// piece through a 128-byte-swizzled shared-memory buffer, which one TMA store
+// writes out, or, for head splits the store's box cannot express, the
+// threads themselves with whole 128-byte row segments per instruction).  The
+// stores travel by TMA rather than through L1, whose bandwidth the MMAs'
+// operand reads share.
 // Up to three problems of one shape share a launch, which is how the Q, K
 // and V projections of self-attention run as one launch.
 //
@@ -28,6 +31,8 @@
 // A tiles in L2).  Two 256-column
 // accumulators in tensor memory alternate, so one tile's epilogue drains
 // while the next tile's MMAs run, and the TMA ring runs on across tiles.
+// Launched with programmatic dependent launch: the kernel sets itself up
+// while the launch before it finishes, and waits for it before touching data.
 #include "internal.h"
 #include "ptx.cuh"
 #include "ptx_cluster.cuh"
@@ -134,7 +139,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
   // the launch that follows may set itself up from here on; every access to
-  // data an earlier launch produced (A, the residual, C) comes after it ends
+  // data an earlier launch may touch (A, and C it may still read) comes after
+  // it ends
   pdl_launch_dependents();
   pdl_wait();
 

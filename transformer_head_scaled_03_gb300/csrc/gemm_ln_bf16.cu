@@ -44,7 +44,9 @@
 // Warp roles: warp 0 TMA producer, warp 1 MMA issuer and TMEM owner (the
 // even CTA's issues for the pair), warps 2-9 epilogue.  One accumulator: the
 // next tile's MMAs wait for the epilogue (of both CTAs), while the TMA ring
-// keeps loading ahead.
+// keeps loading ahead.  Launched with programmatic dependent launch: the
+// kernel sets itself up while the launch before it finishes, and waits for it
+// before touching A, the residual or C.
 #include "internal.h"
 #include "ptx.cuh"
 #include "ptx_cluster.cuh"
